@@ -1,0 +1,558 @@
+#!/usr/bin/env python3
+"""Bucket-flush bandwidth of the ZeRO-1 gradient-reduction path on GB300.
+
+One step = one ZeRO-1 gradient flush of the 402.8M-parameter model at W=8:
+the owner map, then the 7 reduce buckets (52,428,800-element capacity, reverse
+layer order) flushed with reduce-to-owner, probe counters on.  The bf16
+gradients of the 8 replicas ([8, 402,753,536], 6.4 GB) sit in HBM before the
+timed region; every step reads all of them, so no step is served from L2.
+
+Printed (rank 0, one JSON line): whole-job algorithmic HBM GB/s (value),
+grad-elements/s, the roofline of the flush kernel, the same metric end to end
+with host buffers (e2e), the CPU oracle baseline, clocks, and the other hot-path
+rows (AllReduce form, deferred accumulation, ReduceScatter, AllGather) timed on
+their own workloads.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "bucket-flush achieved HBM GB/s and % of GB300 peak; grad-elems/s at W=8"
+WORKLOAD = "zero1-bucket-flush 402.8M params W=8 bf16 reduce-to-owner (7 buckets of <=52,428,800 elems)"
+FALLBACK_HBM_GBS = 6800.0
+SEED, SIGMA, WORLD = 3, 1e-3, 8
+KERNEL_SOURCES = ["flush_kernels.cuh", "flush_bf16.cu", "common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["dpred", "reference"], default="dpred")
+    ap.add_argument("--max-buckets", type=int, default=0, help="flush only the first k buckets (small profiling case)")
+    ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers ---
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "zero_collectives_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch():
+    """dram read+write bytes per flush launch from the committed ncu summary,
+    or None when the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "flush_402m_w8_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("kernel_hash") != kernel_hash():
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling (every 50 ms) around the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        out_dir = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv", dir=out_dir)
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50", "-f", self.path],
+                                         stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(gpus: int):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------- the workload ---
+
+def flush_workload(max_buckets: int):
+    from datagen import workloads
+    tree = workloads.tree_402m()
+    layout = workloads.arrival_layout(tree)
+    buckets = layout.buckets if max_buckets <= 0 else layout.buckets[:max_buckets]
+    return tree, layout, buckets
+
+
+def flush_bytes(world, buckets, omap, holders_written_fn, in_size=2, out_size=2) -> int:
+    """Algorithmic bytes of a flush: every row of every bucket read once, every
+    delivered non-empty destination written once."""
+    total = 0
+    for b in buckets:
+        total += world * b.size * in_size
+        for t in b.tasks:
+            total += int(t["numel"]) * out_size * holders_written_fn(int(t["param_id"]))
+    return total
+
+
+def owner_mode_writes(omap):
+    def n(p):
+        if omap.owner[p] >= 0:
+            return 1
+        return int(omap.holder_hi[p] - omap.holder_lo[p] + 1)
+    return n
+
+
+def events(n):
+    import torch
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def run_dpred(args):
+    import numpy as np
+    import torch
+
+    import datagen
+    import zero_collectives_gb300 as zc
+    from datagen import BF16, NORMAL
+
+    ws, rank, local = dist_setup(args.gpus)
+    tree, layout, buckets = flush_workload(args.max_buckets)
+    n_rows = tree.total
+    stream = torch.cuda.current_stream()
+    grads = torch.empty((WORLD, n_rows), dtype=torch.bfloat16, device="cuda")
+    datagen.fill_device(grads.data_ptr(), WORLD, n_rows, n_rows, BF16, NORMAL, SEED, 0, 1, 0, SIGMA,
+                        stream.cuda_stream)
+    bucket_list = [(b.start, b.tasks) for b in buckets]
+    ex = zc.Zero1Executor(WORLD, tree.numel, layout.row_offset, bucket_list, torch.bfloat16)
+    step_bytes = flush_bytes(WORLD, buckets, ex.omap, owner_mode_writes(ex.omap))
+    step_elems = sum(b.size for b in buckets)
+    launches_per_step = len(buckets)
+
+    def step():
+        zc.build_owner_map(WORLD, [(None, tree.numel)], True)   # the owner map (host, identical every time)
+        ex.flush_all(grads, probe=True)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+
+    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    ev_start, ev_end = events(2)
+    per_launch = events(2 * launches_per_step * args.steps)
+    ev_start.record(stream)
+    i = 0
+    for _ in range(args.steps):
+        zc.build_owner_map(WORLD, [(None, tree.numel)], True)
+        for (start, tasks), size, table in zip(ex.buckets, ex.sizes, ex.tables):
+            per_launch[i].record(stream)
+            zc.flush_bucket(grads[:, start:start + size], tasks, ex.omap.owner, table, zc.BF16, True, True,
+                            probe=True, workspace=ex.workspace, stream=stream)
+            per_launch[i + 1].record(stream)
+            i += 2
+    ev_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    elapsed_ms = ev_start.elapsed_time(ev_end)
+    launch_ms = sum(per_launch[j].elapsed_time(per_launch[j + 1]) for j in range(0, len(per_launch), 2))
+    avg_launch_ms = launch_ms / (launches_per_step * args.steps)
+    elapsed_max = max_over_ranks(elapsed_ms, ws)
+    value_gbs = ws * step_bytes * args.steps / (elapsed_max * 1e-3) / 1e9
+    elems_per_s = ws * step_elems * args.steps / (elapsed_max * 1e-3)
+
+    peak, peak_src = peaks()
+    bytes_per_launch = step_bytes / launches_per_step
+    achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
+    traffic = traffic_per_launch()
+    result = {
+        "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Irwin-Hall normal, sigma 1e-3)",
+        "config": {"workload": WORKLOAD, "world": WORLD, "params": tree.n_params, "elems_per_replica": step_elems,
+                   "buckets": len(buckets), "bucket_capacity": 52_428_800, "reduce_to_owner": True, "pre_div": True,
+                   "parallelism": f"{ws} independent replica(s), no inter-GPU exchange",
+                   "l2": "inputs larger than L2: each step reads 6.4 GB of gradients"},
+        "grad_elems_per_s": round(elems_per_s, 1),
+        "pct_of_peak": round(100.0 * value_gbs / ws / peak, 2),
+        "algorithmic_bytes_per_step": step_bytes,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
+                     "kernel": "flush_kernel<8,2,bf16,bf16,FlushArgsInline>", "bytes_per_launch": bytes_per_launch,
+                     "avg_launch_ms": round(avg_launch_ms, 5)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    probe_line = ex.flush_all(grads, probe=True)[0].line(0, zc.BF16, True)
+    result["probe_line"] = probe_line
+    result["owner_map_report"] = ex.omap.report()
+
+    if not args.no_e2e:
+        result["e2e"] = e2e(args, ex, grads, step_bytes, ws)
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(buckets, tree, layout, args.cpu_seconds)
+    if not args.no_rows:
+        del grads
+        result["rows"] = rows(peak)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e(args, ex, grads, step_bytes, ws):
+    """Same metric through the public API with host buffers: every step copies
+    the gradients in from pinned host memory and the reduced gradients out."""
+    import torch
+    import datagen
+    from datagen import BF16, NORMAL
+    host = torch.empty(grads.shape, dtype=torch.bfloat16, pin_memory=True)
+    datagen.fill_host(host.view(torch.int16).numpy().view("uint16"), BF16, NORMAL, SEED, sigma=SIGMA)
+    outs = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in ex.grad.buf]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        grads.copy_(host, non_blocking=True)
+        ex.flush_all(grads, probe=True)
+        for o, b in zip(outs, ex.grad.buf):
+            o.copy_(b, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    a, b = events(2)
+    a.record(stream)
+    for _ in range(args.e2e_steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), ws)
+    h2d = host.numel() * host.element_size()
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    return {"value": round(ws * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "ms_per_step": round(ms / args.e2e_steps, 3)}
+
+
+def _cpu_flush_sample(buckets, tree, seconds):
+    import numpy as np
+    import datagen
+    import oracle
+    from datagen import BF16, NORMAL
+    om = oracle.owner_map(WORLD, [(list(range(WORLD)), tree.numel)], True)
+    done_bytes, done_s, done_elems, n_b = 0, 0.0, 0, 0
+    for b in buckets:
+        host = datagen.host_matrix(WORLD, b.size, BF16, NORMAL, SEED, col0=b.start, sigma=SIGMA)
+        dst = [[None] * len(b.tasks) for _ in range(WORLD)]
+        writes = 0
+        for t, task in enumerate(b.tasks):
+            p = int(task["param_id"])
+            for r in range(om["holder_lo"][p], om["holder_hi"][p] + 1):
+                dst[r][t] = np.empty(int(task["numel"]), np.uint16)
+            writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else om["holder_hi"][p] - om["holder_lo"][p] + 1)
+        t0 = time.perf_counter()
+        oracle.flush(WORLD, host, b.tasks, om["owner"], tree.n_params, dst, BF16, True, True)
+        done_s += time.perf_counter() - t0
+        done_bytes += WORLD * b.size * 2 + writes * 2
+        done_elems += b.size
+        n_b += 1
+        if done_s >= seconds:
+            break
+    return done_bytes, done_s, done_elems, n_b
+
+
+def cpu_baseline(buckets, tree, layout, seconds):
+    """The oracle (single-threaded C) on the same workload: whole buckets in
+    order until `seconds` of flush time have accumulated."""
+    nbytes, secs, elems, nb = _cpu_flush_sample(buckets, tree, seconds)
+    return {"value": round(nbytes / secs / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{nb} of {len(buckets)} buckets ({elems} elements per replica row), single-threaded C oracle",
+            "seconds": round(secs, 2), "grad_elems_per_s": round(elems / secs, 1)}
+
+
+# -------------------------------------------------------- other hot rows ---
+
+def timed(fn, reps, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    a, b = events(2)
+    s = torch.cuda.current_stream()
+    a.record(s)
+    for _ in range(reps):
+        fn()
+    b.record(s)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def rows(peak):
+    import numpy as np
+    import torch
+    import datagen
+    import zero_collectives_gb300 as zc
+    from datagen import BF16, F32, NORMAL, UNIFORM, stream_id, workloads
+
+    out = {}
+    s = torch.cuda.current_stream().cuda_stream
+
+    def entry(ms, nbytes, **kw):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        d = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4), "bytes": nbytes}
+        d.update(kw)
+        return d
+
+    # AllReduce form vs reduce-to-owner, in place over the 8 bucket rows (the
+    # collective as NCCL runs it: result delivered to every row / to one row).
+    tree = workloads.tree_402m()
+    layout = workloads.arrival_layout(tree)
+    n = tree.total
+    g = torch.empty((WORLD, n), dtype=torch.bfloat16, device="cuda")
+    datagen.fill_device(g.data_ptr(), WORLD, n, n, BF16, NORMAL, SEED, 0, 1, 0, SIGMA, s)
+    for rto, name in ((False, "flush_inplace_allreduce"), (True, "flush_inplace_owner")):
+        om = zc.build_owner_map(WORLD, [(None, tree.numel)], rto)
+
+        def f():
+            for b in layout.buckets:
+                zc.flush_bucket(g[:, b.start:b.start + b.size], b.tasks, om.owner, None, zc.BF16, True, rto)
+
+        ms = timed(f, 5)
+        writes = sum(int(tree.numel[p]) * (1 if om.owner[p] >= 0 else WORLD) for p in range(tree.n_params))
+        out[name] = entry(ms, WORLD * n * 2 + writes * 2, workload="402.8M W=8 bf16, 7 buckets, in place")
+    del g
+
+    # Deferred accumulation: W=4, 8 micro-batches, qwen3-0.6b tree, fp32.
+    W, M = 4, 8
+    n = workloads.tree_qwen3_06b().total
+    acc = torch.empty((W, n), dtype=torch.float32, device="cuda")
+    gb = [torch.empty((W, n), dtype=torch.float32, device="cuda") for _ in range(2)]
+    for m, buf in enumerate(gb):
+        datagen.fill_device(buf.data_ptr(), W, n, n, F32, NORMAL, 4, stream_id(0, m), 1, 0, SIGMA, s)
+    total = torch.empty(n, dtype=torch.float32, device="cuda")
+
+    def deferred():
+        for m in range(M):
+            last = m == M - 1
+            zc.accumulate_microbatch(acc, gb[m % 2], first=(m == 0), finalize=last, total=total if last else None)
+
+    ms = timed(deferred, 3, warm=1)
+    nbytes = 8 * W * n + (M - 2) * 12 * W * n + 8 * W * n + 4 * n
+    out["accumulate_deferred_step"] = entry(ms, nbytes, workload="qwen3-0.6b tree n=596,049,920, W=4, 8 micro-batches, fp32",
+                                            launches=M)
+    addm = lambda: zc.accumulate_microbatch(acc, gb[0], first=False, finalize=False)  # noqa: E731
+    ms_add = timed(addm, 5)
+    out["accumulate_one_microbatch"] = entry(ms_add, 12 * W * n, workload="one acc += g pass, W=4, fp32")
+    fin = lambda: zc.accumulate_microbatch(acc, gb[0], first=False, finalize=True, total=total)  # noqa: E731
+    ms_fin = timed(fin, 5)
+    out["accumulate_finalize"] = entry(ms_fin, 8 * W * n + 4 * n, workload="last micro-batch fused with the reduce")
+    # per-micro-batch all-reduce (the status quo): reduce each micro-batch, then sum
+    red = torch.empty((1, n), dtype=torch.float32, device="cuda")
+    s_m = torch.empty(n, dtype=torch.float32, device="cuda")
+
+    def per_mb():
+        for m in range(M):
+            zc.accumulate_microbatch(acc, gb[m % 2], first=True, finalize=True, total=s_m)
+            zc.accumulate_microbatch(red, s_m.view(1, n), first=(m == 0), finalize=False)
+
+    ms_pm = timed(per_mb, 3, warm=1)
+    out["accumulate_per_microbatch_step"] = entry(ms_pm, M * (4 * W * n + 4 * n) + 4 * n + (M - 1) * 12 * n,
+                                                  workload="status quo: reduce every micro-batch", launches=2 * M)
+    del acc, gb, total, red, s_m
+
+    # ReduceScatter / AllGather, M = 1 GiB bf16.
+    Mel = 1 << 29
+    for N in (8, 4):
+        S = Mel // N
+        x = torch.empty((N, Mel), dtype=torch.bfloat16, device="cuda")
+        datagen.fill_device(x.data_ptr(), N, Mel, Mel, BF16, UNIFORM, 5, 0, 1, 0, 1.0, s)
+        rs = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
+        ms = timed(lambda: zc.reduce_scatter(x, rs), 10)
+        out[f"reduce_scatter_N{N}"] = entry(ms, N * Mel * 2 + Mel * 2, workload=f"N={N}, M=1 GiB bf16")
+        del x
+        ag = torch.empty((N, Mel), dtype=torch.bfloat16, device="cuda")
+        for order, name in ((0, "canonical"), (1, "ring")):
+            ms = timed(lambda: zc.allgather(rs, ag, order), 10)
+            out[f"allgather_{name}_N{N}"] = entry(ms, Mel * 2 + N * Mel * 2, workload=f"N={N}, M=1 GiB bf16")
+        del ag, rs
+    torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------ reference (oracle) ---
+
+def run_reference(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import datagen
+    import oracle
+    from datagen import BF16, NORMAL
+    tree, layout, buckets = flush_workload(args.max_buckets)
+    b = buckets[0]
+    om = oracle.owner_map(WORLD, [(list(range(WORLD)), tree.numel)], True)
+    # Sample per step: the leading tasks of the first bucket, sized so that
+    # warm-up plus timed steps take about two minutes of oracle time.
+    calib = _sub_bucket(b, 1 << 20)
+    host_c = datagen.host_matrix(WORLD, int(calib["offset"][-1] + calib["numel"][-1]), BF16, NORMAL, SEED,
+                                 col0=b.start, sigma=SIGMA)
+    t0 = time.perf_counter()
+    _oracle_step(host_c, calib, om, tree)
+    rate = (1 << 20) / (time.perf_counter() - t0)
+    total_steps = args.steps + max(args.warmup, 1)
+    elems = int(max(8192, min(b.size, rate * 120.0 / total_steps)))
+    tasks = _sub_bucket(b, elems)
+    width = int(tasks["offset"][-1] + tasks["numel"][-1])
+    host = datagen.host_matrix(WORLD, width, BF16, NORMAL, SEED, col0=b.start, sigma=SIGMA)
+    for _ in range(max(args.warmup, 1)):
+        _oracle_step(host, tasks, om, tree)
+    t0 = time.perf_counter()
+    nbytes = 0
+    for _ in range(args.steps):
+        nbytes += _oracle_step(host, tasks, om, tree)
+    secs = time.perf_counter() - t0
+    gbs = nbytes / secs / 1e9
+    sample = f"first {width} elements per replica row of bucket 0 (of 402,753,536), per step; single-threaded C oracle"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate, bf16 I/O",
+        "data": "synthetic (seeded Irwin-Hall normal, sigma 1e-3)",
+        "config": {"workload": WORKLOAD, "world": WORLD, "sample_elems_per_step": width},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def _sub_bucket(b, elems):
+    import numpy as np
+    keep = []
+    acc = 0
+    for t in b.tasks:
+        if acc >= elems:
+            break
+        t = t.copy()
+        t["numel"] = min(int(t["numel"]), elems - acc)
+        keep.append(t)
+        acc += int(t["numel"])
+    return np.array(keep, dtype=b.tasks.dtype)
+
+
+def _oracle_step(host, tasks, om, tree):
+    import numpy as np
+    import oracle
+    from datagen import BF16
+    dst = [[None] * len(tasks) for _ in range(WORLD)]
+    writes = 0
+    for t, task in enumerate(tasks):
+        p = int(task["param_id"])
+        for r in range(om["holder_lo"][p], om["holder_hi"][p] + 1):
+            dst[r][t] = np.empty(int(task["numel"]), np.uint16)
+        writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else om["holder_hi"][p] - om["holder_lo"][p] + 1)
+    oracle.flush(WORLD, host, tasks, om["owner"], tree.n_params, dst, BF16, True, True)
+    return WORLD * host.shape[1] * 2 + writes * 2
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_dpred(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+/*
+ * dpred.h -- C ABI of libdpred: data-parallel gradient reduction (ZeRO-1 bucket
+ * flush, deferred accumulation, ReduceScatter / AllGather) on one GPU.
+ *
+ * The W data-parallel replicas are W rows of one array in device memory.  Each
+ * "collective" of the pages becomes one streaming kernel over those rows:
+ * Reduce -> written to one destination, AllReduce -> written to every
+ * destination, ReduceScatter / AllGather -> reduce-and-shard / copy layouts.
+ *
+ * Pages this interface follows (cited by title and section):
+ *  [DS] DeepSpeed issue #8700 "[REQUEST] DeepCompile ZeRO-1: reduce-to-owner
+ *       instead of AllReduce".
+ *  [MT] MaxText PR #5099 "Defer the data-parallel gradient all-reduce to
+ *       update() under gradient accumulation".
+ *  [AG] "AllGather" (tier6-model interconnect notes, 集合通信 / all-gather).
+ *
+ * Conventions shared by every call:
+ *  - Return value: DPRED_OK (0) or a negative DPRED_E_* code.  Nothing aborts
+ *    or traps.  dpred_last_error() gives this thread's message for the last
+ *    failure.  Arguments are validated before any device work is enqueued; a
+ *    call that fails validation enqueues nothing.
+ *  - Memory: the caller owns all memory; the library allocates no device
+ *    memory.  "device" pointers are CUDA device (or managed) addresses,
+ *    "host" pointers are ordinary process memory read during the call only.
+ *  - Element types: DPRED_BF16 (bfloat16, 2 bytes) and DPRED_F32 (4 bytes).
+ *    Every data pointer must be aligned to its element size (DPRED_E_ALIGN);
+ *    16-byte alignment is not required but enables the vectorised path.
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *    Device work is enqueued on it and the call returns without waiting.
+ *  - Arithmetic of every reduction: each term is widened to fp32, optionally
+ *    pre-divided by the number of ranks (IEEE division), and the terms are
+ *    summed in fp32 in rank order 0, 1, ..., W-1 starting from the rank-0
+ *    term; the sum is rounded once to the output type (bf16: round to
+ *    nearest, ties to even).  The order never depends on the launch shape, so
+ *    results are bitwise reproducible.
+ */
+#ifndef DPRED_H
+#define DPRED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define DPRED_OK 0
+#define DPRED_E_INVAL (-1)    /* bad argument (null pointer, bad dtype, negative size, ...) */
+#define DPRED_E_ALIGN (-2)    /* a pointer is not aligned to its element size */
+#define DPRED_E_SIZE (-3)     /* sizes inconsistent (range outside a row, M % N != 0, workspace too small) */
+#define DPRED_E_MISMATCH (-4) /* checked mode: destinations disagree with the owner map */
+#define DPRED_E_CUDA (-5)     /* a CUDA runtime call failed */
+#define DPRED_E_TIMEOUT (-6)  /* a device-side bounded wait gave up (reported by dpred_device_status) */
+
+/* element types */
+#define DPRED_BF16 0
+#define DPRED_F32 1
+
+#define DPRED_MAX_WORLD 64
+
+/* One parameter group ([DS] "Design points": param groups; groups reduced
+ * over another communicator are excluded from the owner map). */
+typedef struct {
+    int32_t comm_size;          /* ranks of the group's communicator */
+    int32_t n_params;           /* parameters in the group */
+    const int32_t* comm_ranks;  /* host [comm_size]: group rank -> data-parallel rank; NULL = identity */
+    const int64_t* numel;       /* host [n_params]: sizes in the group's flat (model) order */
+} dpred_group;
+
+/* One task of a reduce bucket: one whole parameter gradient ([DS] "Describe
+ * alternatives you've considered": buckets are assembled in gradient-arrival
+ * order, one full-parameter task each).  24 bytes. */
+typedef struct {
+    int32_t param_id;  /* index into the owner map */
+    int32_t reserved;  /* must be 0 */
+    int64_t offset;    /* element offset of the task inside every bucket row */
+    int64_t numel;     /* elements */
+} dpred_task;
+
+/* Probe counters of one flush ([DS] "reduce_probe" and the printed probe
+ * line).  discarded% of rank r = 100 * (reduced_elems - kept_elems[r]) /
+ * reduced_elems; owner% = 100 * owner_elems / reduced_elems. */
+typedef struct {
+    int64_t flush_index;    /* in: caller's flush counter, copied through unchanged */
+    int64_t tasks;          /* tasks in the bucket */
+    int64_t reduced_elems;  /* sum of task sizes */
+    int64_t owner_tasks;    /* tasks that took the reduce-to-owner path */
+    int64_t owner_elems;    /* their elements */
+    int64_t kept_elems[DPRED_MAX_WORLD]; /* per rank: elements of tasks whose destination is non-empty */
+} dpred_probe;
+
+const char* dpred_last_error(void);
+const char* dpred_version(void);
+
+/*
+ * Owner map.  [DS] "Design points" ("Owner map costs nothing to build",
+ * "Partial parameters keep AllReduce", "No native flag", "Parameter groups
+ * reduced over a different communicator are skipped").
+ *
+ * Each group's flat space of T elements is cut into comm_size contiguous
+ * partitions of ceil(T / comm_size) elements (the last one shorter).  A
+ * parameter covering [s, e) is held by partitions lo = s / P .. hi = (e-1) / P.
+ * owner[p] = lo when lo == hi, the group is eligible and reduce_to_owner != 0;
+ * otherwise -1 (AllReduce).  Eligible: comm_size == world and comm_ranks[i] == i.
+ * For an ineligible group owner = -1 and every data-parallel rank is treated
+ * as a holder (holder_lo = 0, holder_hi = world - 1); a zero-size parameter
+ * has owner = holder_lo = holder_hi = -1.  The result does not depend on
+ * `rank` (the map is identical on every rank).
+ *
+ * Host only, synchronous.  Outputs (host, caller-allocated) are indexed by
+ * parameter in group order then flat order: owner, holder_lo, holder_hi
+ * [sum n_params]; *n_owned = parameters with an owner, *n_total = all
+ * parameters (the "k/total gradients reduce to one rank" report).
+ * Errors: DPRED_E_INVAL for world outside 1..DPRED_MAX_WORLD, rank outside
+ * 0..world-1, negative sizes or null pointers.
+ */
+int dpred_build_owner_map(int32_t world, int32_t rank, const dpred_group* groups, int32_t n_groups,
+                          int32_t reduce_to_owner, int32_t* owner, int32_t* holder_lo, int32_t* holder_hi,
+                          int32_t* n_owned, int32_t* n_total);
+
+/*
+ * Probe counters of a flush from its metadata alone, without launching
+ * anything ([DS] "reduce_probe": size the win before turning the path on).
+ * Arguments as for dpred_flush_bucket.  kept_elems[r] sums the tasks whose
+ * rank-r destination dst[r * n_tasks + t] is non-NULL; with dst == NULL (in
+ * place) it sums the tasks delivered to row r.  probe->flush_index is left as
+ * the caller set it.  Host only.
+ */
+int dpred_flush_probe(int32_t world, const dpred_task* tasks, int32_t n_tasks, const int32_t* owner,
+                      int32_t n_params, void* const* dst, int32_t reduce_to_owner, dpred_probe* probe);
+
+/*
+ * Device workspace (bytes) that dpred_flush_bucket may need for a bucket of
+ * n_tasks tasks at this world size.  Buckets of up to 128 tasks with up to
+ * 512 written destinations travel inside the kernel launch and need none; for
+ * larger ones the task table is copied (host -> device, from pageable memory,
+ * so such a call waits for the copy to be staged) into the workspace.
+ */
+size_t dpred_flush_workspace_bytes(int32_t world, int32_t n_tasks);
+
+/*
+ * ZeRO-1 bucket flush.  [DS] "Describe the solution you'd like" (for a
+ * parameter inside one partition, reduce to the single rank that keeps it:
+ * same reduction, same operand order, one destination instead of ws), design
+ * points "Partial parameters keep AllReduce", "Copy-out is unchanged and
+ * still correct" and "Summation semantics untouched" (pre-division by the
+ * world size before the sum), and the copy-out loop that skips empty buffers.
+ *
+ * grads (device) is the bucket: `world` rows of in_dtype elements, row r
+ * starting at element r * ld.  Task t reduces elements
+ * [offset, offset + numel) of every row.  root(t) = owner[param_id] when
+ * reduce_to_owner != 0 and owner != NULL and it is >= 0, else -1.  The
+ * reduced values go to rank root(t) only (root >= 0) or to every rank
+ * (root == -1, the AllReduce fallback), and to a delivered rank r only if
+ * its destination is non-empty:
+ *  - dst != NULL: host array [world * n_tasks] of device pointers;
+ *    dst[r * n_tasks + t] is rank r's buffer for task t (numel out_dtype
+ *    elements) or NULL for an empty buffer.  Buffers of ranks that are not
+ *    delivered are never touched.
+ *  - dst == NULL: in place; the result overwrites the task's range in the
+ *    delivered rows of grads.  out_dtype must equal in_dtype and tasks must
+ *    not overlap.
+ * owner: host [n_params] or NULL (no owners: AllReduce everything, the
+ * flag-off path).  pre_div != 0 divides every term by world.  checked != 0
+ * additionally verifies that an owner task has no non-NULL destination on a
+ * rank other than its owner (DPRED_E_MISMATCH).  probe (host, may be NULL)
+ * receives the counters of dpred_flush_probe.  workspace (device, may be NULL
+ * when dpred_flush_workspace_bytes() is 0) of workspace_bytes bytes.
+ * Asynchronous on `stream`; grads, dst buffers and workspace must stay valid
+ * until the work completes.  Errors: DPRED_E_INVAL, DPRED_E_ALIGN,
+ * DPRED_E_SIZE (a task outside [0, ld), overlapping in-place tasks, workspace
+ * too small), DPRED_E_MISMATCH, DPRED_E_CUDA.
+ */
+int dpred_flush_bucket(int32_t world, int32_t in_dtype, void* grads, int64_t ld, const dpred_task* tasks,
+                       int32_t n_tasks, const int32_t* owner, int32_t n_params, int32_t out_dtype, void* const* dst,
+                       int32_t pre_div, int32_t reduce_to_owner, int32_t checked, dpred_probe* probe,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Replica-local gradient accumulation with one cross-replica reduction per
+ * optimizer step.  [MT] "What" (cotangents come out unreduced, a per-replica
+ * partial sum that accumulates replica-locally across micro-batches; update()
+ * emits the single cross-replica all-reduce).
+ *
+ * acc (device, fp32) and g (device, g_dtype) are [world, n], row-contiguous.
+ * For every replica r and element k:  a = first ? g[r][k] : acc[r][k] + g[r][k].
+ *  - finalize == 0: acc[r][k] = a.
+ *  - finalize != 0: total[k] = (a[0] + a[1] + ... + a[world-1]) * scale (rank
+ *    order, fp32), total (device, fp32, [n]); acc is not written (the
+ *    accumulator is consumed by the reduction), so the last micro-batch's add
+ *    and the cross-replica reduction are one pass.
+ * scale multiplies the finished sum (e.g. 1 / denominator; 1.0 leaves it
+ * unchanged).  Asynchronous on `stream`.  Errors: DPRED_E_INVAL (null
+ * pointer, bad dtype, n < 0, world outside 1..DPRED_MAX_WORLD),
+ * DPRED_E_ALIGN, DPRED_E_CUDA.
+ */
+int dpred_accumulate_microbatch(int32_t world, int64_t n, float* acc, int32_t g_dtype, const void* g,
+                                int32_t first, int32_t finalize, float scale, float* total, void* stream);
+
+/*
+ * ReduceScatter.  [AG] "与 ReduceScatter 的对偶关系" (duality table: M
+ * elements in per node, M/N out per node, reduce then shard).
+ * in (device) is [n_nodes, m_elems] of in_dtype; out (device) is
+ * [n_nodes, m_elems / n_nodes] of out_dtype; out[i][k] is the reduction of
+ * in[0..N-1][i * S + k], S = m_elems / n_nodes (pre_div divides every term by
+ * n_nodes).  Errors: DPRED_E_SIZE when m_elems % n_nodes != 0, DPRED_E_INVAL,
+ * DPRED_E_ALIGN, DPRED_E_CUDA.  Asynchronous on `stream`.
+ */
+int dpred_reduce_scatter(int32_t n_nodes, int64_t m_elems, int32_t in_dtype, const void* in, int32_t out_dtype,
+                         void* out, int32_t pre_div, void* stream);
+
+/*
+ * AllGather.  [AG] "语义定义" (eq. ag-semantic-output: every node ends with
+ * B_i = [A_0, A_1, ..., A_{N-1}]) and "Ring AllGather" (the N=4 table: after
+ * the ring schedule node i holds [A_i, A_{i-1}, ..., A_{i-N+1}], indices mod N).
+ * in (device) is [n_nodes, shard_elems] (row j = A_j); out (device) is
+ * [n_nodes, n_nodes * shard_elems]:
+ *   order 0 (canonical): out[i][c * S + k] = in[c][k]
+ *   order 1 (ring):      out[i][c * S + k] = in[(i - c) mod N][k]
+ * A bit copy: the element type only sets the element size.  Errors:
+ * DPRED_E_INVAL (order not 0/1, ...), DPRED_E_ALIGN, DPRED_E_CUDA.
+ * Asynchronous on `stream`.
+ */
+int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const void* in, void* out, int32_t order,
+                    void* stream);
+
+/*
+ * Device error word: 0, or the DPRED_E_* code of the first device-side
+ * failure (a bounded wait that gave up, an internal consistency check) since
+ * the last clear.  Synchronises the current device.  clear != 0 resets it.
+ */
+int dpred_device_status(int32_t* code, int32_t clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPRED_H */

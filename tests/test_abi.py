@@ -1,0 +1,198 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point its
+header declares, and its host-only entry points (owner map, probe counters,
+argument validation) agree with the oracle.  No call here launches a kernel:
+the device entry points are only called with arguments they must reject."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import zero_collectives_gb300 as zc
+from datagen import workloads
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def L():
+    from zero_collectives_gb300 import build
+    build.build()
+    return zc.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "dpred.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dpred_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(L, n), n
+    assert zc.version().startswith("dpred")
+
+
+def test_owner_map_matches_oracle_402m(L):
+    tree = workloads.tree_402m()
+    for rto in (True, False):
+        got = zc.build_owner_map(8, [(None, tree.numel)], rto)
+        ref = oracle.owner_map(8, [(list(range(8)), tree.numel)], rto)
+        for k in ("owner", "holder_lo", "holder_hi"):
+            assert np.array_equal(getattr(got, k), ref[k])
+        assert (got.n_owned, got.n_total) == (ref["n_owned"], ref["n_total"])
+    assert zc.build_owner_map(8, [(None, tree.numel)]).report() == \
+        "DeepCompile reduce_to_owner: 236/243 gradients reduce to one rank"
+
+
+def test_owner_map_matches_oracle_random_groups(L):
+    rng = np.random.default_rng(12)
+    for _ in range(300):
+        world = int(rng.integers(1, 17))
+        groups_o, groups_z = [], []
+        for g in range(int(rng.integers(1, 4))):
+            sizes = rng.integers(0, 5000, size=int(rng.integers(0, 30)))
+            kind = rng.integers(0, 3)
+            ranks = list(range(world))
+            if kind == 1 and world > 1:
+                ranks = list(range(max(1, world // 2)))
+            elif kind == 2 and world > 1:
+                ranks = ranks[::-1]
+            groups_o.append((ranks, sizes))
+            groups_z.append((ranks, sizes))
+        rank = int(rng.integers(0, world))
+        got = zc.build_owner_map(world, groups_z, True, rank)
+        ref = oracle.owner_map(world, groups_o, True, rank)
+        for k in ("owner", "holder_lo", "holder_hi"):
+            assert np.array_equal(getattr(got, k), ref[k])
+        assert (got.n_owned, got.n_total) == (ref["n_owned"], ref["n_total"])
+
+
+def test_probe_counters_match_oracle(L):
+    tree = workloads.tree_402m()
+    om = zc.build_owner_map(8, [(None, tree.numel)])
+    layout = workloads.arrival_layout(tree)
+    for b in layout.buckets:
+        n = len(b.tasks)
+        ptrs = []
+        has = np.zeros((8, n), bool)
+        for r in range(8):
+            for t in range(n):
+                p = int(b.tasks["param_id"][t])
+                held = om.holder_lo[p] <= r <= om.holder_hi[p]
+                has[r, t] = held
+                ptrs.append(0x1000 + 16 * (r * n + t) if held else 0)
+        table = zc.DstTable(8, n, ptrs)
+        for rto in (True, False):
+            got = zc.flush_probe(8, b.tasks, om.owner, table, rto, flush_index=5)
+            ref = oracle.flush_probe(8, b.tasks, om.owner, tree.n_params, has, rto)
+            assert got.flush_index == 5
+            assert (got.tasks, got.reduced_elems, got.owner_tasks, got.owner_elems) == \
+                (ref["tasks"], ref["reduced_elems"], ref["owner_tasks"], ref["owner_elems"])
+            assert got.kept_elems == ref["kept_elems"]
+        inplace = zc.flush_probe(8, b.tasks, om.owner, None, True)
+        ref = oracle.flush_probe(8, b.tasks, om.owner, tree.n_params, None, True)
+        assert inplace.kept_elems == ref["kept_elems"]
+
+
+def test_probe_line_reproduces_printed_line(golden_dir, L):
+    meta, line = {}, None
+    for raw in open(os.path.join(golden_dir, "probe_line.txt")):
+        raw = raw.rstrip("\n")
+        if raw.startswith("[dc-probe]"):
+            line = raw
+        elif raw and not raw.startswith("#"):
+            k, v = raw.split("=")
+            meta[k] = int(v)
+    world = meta["world"]
+    per = 52_428_800 // world
+    sizes = []
+    for j in range(world):
+        k = 15 if j < 6 else 14
+        base = per // k
+        sizes += [base] * (k - 1) + [per - base * (k - 1)]
+    tree = workloads.Tree([f"p{i}" for i in range(len(sizes))], np.array(sizes, np.int64))
+    b = workloads.arrival_layout(tree, capacity=None).buckets[0]
+    om = zc.build_owner_map(world, [(None, tree.numel)], reduce_to_owner=False)
+    n = len(b.tasks)
+    ptrs = [0x1000 if om.holder_lo[int(b.tasks["param_id"][t])] <= r <= om.holder_hi[int(b.tasks["param_id"][t])]
+            else 0 for r in range(world) for t in range(n)]
+    pr = zc.flush_probe(world, b.tasks, om.owner, zc.DstTable(world, n, ptrs), False, flush_index=meta["flush_index"])
+    assert pr.line(meta["rank"], zc.BF16, True) == line
+    log = []
+    plog = zc.ProbeLog(rank=0, limit=20, sink=log.append)
+    for i in range(25):
+        pr.flush_index = plog.next_index()
+        plog.record(pr, zc.BF16, True)
+    assert len(log) == 20
+
+
+def _tasks(spec):
+    t = np.zeros(len(spec), dtype=zc.TASK_DTYPE)
+    for i, (p, o, n) in enumerate(spec):
+        t[i] = (p, 0, o, n)
+    return t
+
+
+def _call_flush(L, world=4, in_dt=0, grads=0x10000, ld=100, tasks=None, owner=None, n_params=0, out_dt=0,
+                dst=None, checked=0):
+    tasks = _tasks([(0, 0, 10)]) if tasks is None else tasks
+    own = None if owner is None else np.ascontiguousarray(owner, np.int32)
+    return L.dpred_flush_bucket(world, in_dt, grads, ld, tasks.ctypes.data, len(tasks),
+                                None if own is None else own.ctypes.data, n_params if own is not None else 0,
+                                out_dt, dst, 1, 1, checked, None, None, 0, None)
+
+
+def test_validation_rejects_before_launch(L):
+    E = {"INVAL": -1, "ALIGN": -2, "SIZE": -3, "MISMATCH": -4}
+    assert _call_flush(L, world=0) == E["INVAL"]
+    assert _call_flush(L, world=65) == E["INVAL"]
+    assert _call_flush(L, in_dt=7) == E["INVAL"]
+    assert _call_flush(L, ld=5) == E["SIZE"]                              # task outside the row
+    assert _call_flush(L, grads=0x10001) == E["ALIGN"]                    # bf16 needs 2-byte alignment
+    assert _call_flush(L, grads=0) == E["INVAL"]
+    assert _call_flush(L, out_dt=1) == E["INVAL"]                         # in place needs equal dtypes
+    assert _call_flush(L, tasks=_tasks([(0, 0, 10), (1, 5, 10)]), ld=100) == E["SIZE"]  # overlap in place
+    assert _call_flush(L, tasks=_tasks([(3, 0, 10)]), owner=[0, 1], n_params=2) == E["INVAL"]
+    assert _call_flush(L, tasks=_tasks([(0, 0, 10)]), owner=[9], n_params=1) == E["INVAL"]  # owner not a rank
+    bad = _tasks([(0, -1, 10)])
+    assert _call_flush(L, tasks=bad) == E["INVAL"]
+    # checked mode: an owned task with a buffer on a non-owner rank
+    tbl = (ctypes.c_void_p * 4)(0x20000, 0x30000, None, None)
+    assert _call_flush(L, tasks=_tasks([(0, 0, 10)]), owner=[0], n_params=1, dst=tbl, checked=1) == E["MISMATCH"]
+    assert b"owned by rank 0" in L.dpred_last_error()
+    # reduce-scatter / allgather / accumulate argument checks
+    assert L.dpred_reduce_scatter(4, 10, 0, 0x1000, 0, 0x2000, 0, None) == E["SIZE"]
+    assert L.dpred_reduce_scatter(0, 8, 0, 0x1000, 0, 0x2000, 0, None) == E["INVAL"]
+    assert L.dpred_allgather(4, 8, 0, 0x1000, 0x2000, 2, None) == E["INVAL"]
+    assert L.dpred_allgather(4, 8, 0, 0x1001, 0x2000, 0, None) == E["ALIGN"]
+    assert L.dpred_accumulate_microbatch(4, -1, 0x1000, 0, 0x2000, 1, 0, ctypes.c_float(1.0), None, None) == E["INVAL"]
+    assert L.dpred_accumulate_microbatch(4, 8, 0x1000, 0, 0x2000, 1, 1, ctypes.c_float(1.0), None, None) == E["INVAL"]
+    assert L.dpred_accumulate_microbatch(4, 8, 0x1002, 0, 0x2000, 1, 0, ctypes.c_float(1.0), None, None) == E["ALIGN"]
+
+
+def test_empty_calls_are_no_ops(L):
+    # zero tasks / zero elements enqueue nothing and succeed without a GPU
+    t = np.zeros(0, dtype=zc.TASK_DTYPE)
+    assert L.dpred_flush_bucket(4, 0, None, 0, t.ctypes.data, 0, None, 0, 0, None, 1, 1, 0, None, None, 0, None) == 0
+    assert L.dpred_flush_workspace_bytes(8, 64) == 0          # 512 destinations at most: inline
+    assert L.dpred_flush_workspace_bytes(8, 100) == 100 * 32 + 8 * 100 * 8
+    assert L.dpred_flush_workspace_bytes(2, 200) == 200 * 32 + 2 * 200 * 8
+
+
+def test_owner_map_argument_errors(L):
+    own = np.zeros(2, np.int32)
+    g = (zc._Group * 1)()
+    n = np.array([5, 5], np.int64)
+    g[0].comm_size, g[0].n_params, g[0].comm_ranks, g[0].numel = 2, 2, None, n.ctypes.data
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    assert L.dpred_build_owner_map(2, 2, g, 1, 1, own.ctypes.data, own.ctypes.data, own.ctypes.data,
+                                   ctypes.byref(a), ctypes.byref(b)) == -1   # rank outside the world
+    assert L.dpred_build_owner_map(0, 0, g, 1, 1, own.ctypes.data, own.ctypes.data, own.ctypes.data,
+                                   ctypes.byref(a), ctypes.byref(b)) == -1
+    n[1] = -3
+    assert L.dpred_build_owner_map(2, 0, g, 1, 1, own.ctypes.data, own.ctypes.data, own.ctypes.data,
+                                   ctypes.byref(a), ctypes.byref(b)) == -1

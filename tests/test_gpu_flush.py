@@ -1,0 +1,212 @@
+"""GPU parity of dpred_flush_bucket against the CPU oracle (bit-exact).
+
+The tiny workload (W=4, 16 parameters of 1..4096 elements, straddlers), a
+sweep of world sizes / dtypes / straddler counts / excluded groups with both
+the 16-byte vector path and the scalar path, the in-place form, the
+workspace plan, and the full 402.8M-parameter W=8 flush in the configuration
+the bench times (sampled outputs checked one by one)."""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+import zero_collectives_gb300 as zc
+from datagen import BF16, F32, NORMAL, workloads
+from tests.gpu_util import TORCH_DT, device_matrix, np_bits, oracle_flush, to_bits
+from tests.helpers import holder_sets, is_sentinel
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 16  # canary elements before and after every destination
+
+
+class SlotBuffers:
+    """One NaN-filled CUDA buffer per (rank, held parameter) with GUARD canary
+    elements on each side; `shift` moves the destination by whole elements
+    (shift 'co' keeps it co-aligned with its source, 'mis' breaks that)."""
+
+    def __init__(self, world, tasks, holders, out_dt, in_dt, mode):
+        vec = 8 if in_dt == BF16 else 4
+        self.world, self.tasks = world, tasks
+        self.buf, self.off = {}, {}
+        ptrs = []
+        for r in range(world):
+            for task in tasks:
+                p, off, n = int(task["param_id"]), int(task["offset"]), int(task["numel"])
+                if r not in holders[p]:
+                    ptrs.append(0)
+                    continue
+                shift = off % vec + (1 if mode == "mis" else 0)
+                b = torch.full((n + 2 * GUARD + vec,), float("nan"), dtype=TORCH_DT[out_dt], device="cuda")
+                self.buf[(r, p)] = b
+                self.off[(r, p)] = GUARD + shift
+                ptrs.append(b.data_ptr() + (GUARD + shift) * b.element_size())
+        self.table = zc.DstTable(world, len(tasks), ptrs)
+
+    def check_against(self, oracle_dst, tasks, out_dt):
+        """Delivered slots equal the oracle bit for bit; the rest and the guards stay NaN."""
+        for t, task in enumerate(tasks):
+            p, n = int(task["param_id"]), int(task["numel"])
+            for r in range(self.world):
+                o = oracle_dst[r][t]
+                if o is None:
+                    assert (r, p) not in self.buf
+                    continue
+                b = self.buf[(r, p)]
+                s = self.off[(r, p)]
+                got = to_bits(b)
+                isn = torch.isnan(b.float()).cpu().numpy()
+                assert isn[:s].all() and isn[s + n:].all(), f"canary overwritten at rank {r} param {p}"
+                if np.all(is_sentinel(o, out_dt == BF16)):
+                    assert isn[s:s + n].all(), f"non-delivered buffer written at rank {r} param {p}"
+                else:
+                    assert np.array_equal(got[s:s + n], np_bits(o)), f"rank {r} param {p}"
+
+
+def run_case(world, groups, in_dt, out_dt, pre_div, rto, mode="co", capacity=None, seed=21, ld_pad=0, sigma=1e-2):
+    numel = np.concatenate([np.asarray(g[1], np.int64) for g in groups])
+    tree = workloads.Tree([f"p{i}" for i in range(len(numel))], numel)
+    layout = workloads.arrival_layout(tree, capacity=capacity)
+    row = tree.total
+    ld = row + ld_pad
+    grads = device_matrix(world, row, in_dt, NORMAL, seed, sigma=sigma, ld=ld)
+    host = datagen.host_matrix(world, row, in_dt, NORMAL, seed, sigma=sigma)
+    zgroups = [(None if list(g[0]) == list(range(world)) else g[0], g[1]) for g in groups]
+    om = zc.build_owner_map(world, zgroups, rto)
+    holders = holder_sets(om.holder_lo, om.holder_hi)
+    for b in layout.buckets:
+        sb = SlotBuffers(world, b.tasks, holders, out_dt, in_dt, mode)
+        probe = zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, sb.table, out_dt, pre_div,
+                                rto, checked=True, probe=True)
+        sub = np.ascontiguousarray(host[:, b.start:b.start + b.size])
+        odst, oom, oprobe = oracle_flush(world, sub, b.tasks, numel, groups, out_dt, pre_div, rto, tree.n_params)
+        assert np.array_equal(oom["owner"], om.owner)
+        torch.cuda.synchronize()
+        sb.check_against(odst, b.tasks, out_dt)
+        assert (probe.tasks, probe.reduced_elems, probe.owner_tasks, probe.owner_elems) == \
+            (oprobe["tasks"], oprobe["reduced_elems"], oprobe["owner_tasks"], oprobe["owner_elems"])
+        assert probe.kept_elems == oprobe["kept_elems"]
+    assert zc.device_status() == 0
+
+
+@pytest.mark.parametrize("rto", [True, False])
+@pytest.mark.parametrize("out_dt", [BF16, F32])
+@pytest.mark.parametrize("mode", ["co", "mis"])
+def test_tiny_workload(rto, out_dt, mode):
+    world = 4
+    tree = workloads.tree_tiny(seed=1)
+    run_case(world, [(list(range(world)), tree.numel)], BF16, out_dt, True, rto, mode=mode, seed=2)
+
+
+@pytest.mark.parametrize("world", [2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("in_dt,out_dt", [(BF16, BF16), (F32, F32), (BF16, F32), (F32, BF16)])
+def test_sweep_world_dtype_straddlers(world, in_dt, out_dt):
+    rng = np.random.default_rng(world * 7 + in_dt * 3 + out_dt)
+    for straddlers in sorted({0, world // 2, world - 1}):
+        elems = int(rng.integers(3, 9)) * 8192 * world + int(rng.integers(0, 999))  # several units + ragged tail
+        tree = workloads.straddle_tree(world, elems, straddlers)
+        groups = [(list(range(world)), tree.numel)]
+        if world >= 4:
+            groups.append((list(range(world // 2)), np.array([777, 4096, 33], np.int64)))  # excluded group
+        for pre_div, rto in ((True, True), (False, False)):
+            run_case(world, groups, in_dt, out_dt, pre_div, rto, mode="co", seed=30 + straddlers)
+    run_case(world, [(list(range(world)), workloads.straddle_tree(world, 5000 * world + 7, world - 1).numel)],
+             in_dt, out_dt, True, True, mode="mis", seed=41, ld_pad=5)
+
+
+def test_many_tasks_use_the_workspace_plan():
+    world = 8
+    sizes = np.array([(i * 37) % 500 + 1 for i in range(300)], np.int64)
+    assert zc.flush_workspace_bytes(world, 300) > 0
+    tree = workloads.Tree([f"p{i}" for i in range(300)], sizes)
+    layout = workloads.arrival_layout(tree, capacity=None)
+    b = layout.buckets[0]
+    grads = device_matrix(world, tree.total, BF16, NORMAL, 7, sigma=1e-2)
+    host = datagen.host_matrix(world, tree.total, BF16, NORMAL, 7, sigma=1e-2)
+    om = zc.build_owner_map(world, [(None, sizes)], False)
+    holders = holder_sets(om.holder_lo, om.holder_hi)
+    sb = SlotBuffers(world, b.tasks, holders, BF16, BF16, "co")
+    ws = torch.empty(zc.flush_workspace_bytes(world, len(b.tasks)), dtype=torch.uint8, device="cuda")
+    with pytest.raises(zc.DpredError):
+        zc.flush_bucket(grads, b.tasks, om.owner, sb.table, BF16, True, False)  # no workspace given
+    zc.flush_bucket(grads, b.tasks, om.owner, sb.table, BF16, True, False, workspace=ws)
+    odst, _, _ = oracle_flush(world, host, b.tasks, sizes, [(list(range(world)), sizes)], BF16, True, False, 300)
+    torch.cuda.synchronize()
+    sb.check_against(odst, b.tasks, BF16)
+
+
+@pytest.mark.parametrize("rto", [True, False])
+@pytest.mark.parametrize("dt", [BF16, F32])
+def test_in_place(rto, dt):
+    world = 8
+    tree = workloads.straddle_tree(world, 40000 * world + 13, 5)
+    layout = workloads.arrival_layout(tree, capacity=None)
+    b = layout.buckets[0]
+    grads = device_matrix(world, tree.total, dt, NORMAL, 9, sigma=1e-2)
+    host = datagen.host_matrix(world, tree.total, dt, NORMAL, 9, sigma=1e-2)
+    om = zc.build_owner_map(world, [(None, tree.numel)], rto)
+    probe = zc.flush_bucket(grads, b.tasks, om.owner, None, dt, True, rto, probe=True)
+    oprobe = oracle.flush(world, host, b.tasks, om.owner, tree.n_params, None, dt, True, rto)
+    assert np.array_equal(to_bits(grads), np_bits(host))
+    assert probe.kept_elems == oprobe["kept_elems"]
+
+
+def test_identical_replicas_reproduce_exactly():
+    """The DeepSpeed issue's exactness check: identical input on every rank
+    reproduces the input exactly (bf16, pre-division by a power of two)."""
+    world = 8
+    tree = workloads.tree_tiny(seed=1)
+    row = device_matrix(1, tree.total, BF16, NORMAL, 3, sigma=1e-2)
+    grads = row.repeat(world, 1).contiguous()
+    layout = workloads.arrival_layout(tree, capacity=None)
+    om = zc.build_owner_map(world, [(None, tree.numel)])
+    zc.flush_bucket(grads, layout.buckets[0].tasks, om.owner, None, BF16, True, True)
+    for t in layout.buckets[0].tasks:
+        o, n = int(t["offset"]), int(t["numel"])
+        p = int(t["param_id"])
+        r = om.owner[p] if om.owner[p] >= 0 else 0
+        assert torch.equal(grads[r, o:o + n].view(torch.int16), row[0, o:o + n].view(torch.int16))
+
+
+def test_402m_w8_full_size_sampled():
+    """The full 402.8M-parameter W=8 bf16 flush (7 buckets, reduce-to-owner),
+    run through the executor exactly as the bench times it."""
+    world, sigma, seed = 8, 1e-3, 3
+    tree = workloads.tree_402m()
+    layout = workloads.arrival_layout(tree)
+    grads = device_matrix(world, tree.total, BF16, NORMAL, seed, sigma=sigma)
+    ex = zc.Zero1Executor(world, tree.numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets],
+                          torch.bfloat16, fill=float("nan"))
+    probes = ex.flush_all(grads, probe=True)
+    torch.cuda.synchronize()
+    assert zc.device_status() == 0
+    om = oracle.owner_map(world, [(list(range(world)), tree.numel)])
+    assert np.array_equal(om["owner"], ex.omap.owner)
+    # every delivered slot fully written, nothing else
+    for r in range(world):
+        delivered = sum(int(tree.numel[p]) for p in range(tree.n_params)
+                        if om["owner"][p] == r or (om["owner"][p] < 0 and om["holder_lo"][p] <= r <= om["holder_hi"][p]))
+        written = int((~torch.isnan(ex.grad.buf[r].float())).sum().item())
+        assert written == delivered, f"rank {r}: {written} written, {delivered} delivered"
+    # sampled values, one by one against the oracle
+    rng = np.random.default_rng(0)
+    picks = []
+    for p in range(tree.n_params):
+        n = int(tree.numel[p])
+        ks = {0, n - 1} | set(int(v) for v in rng.integers(0, n, size=24))
+        picks += [(p, k) for k in sorted(ks)]
+    P = np.array([p for p, _ in picks])
+    K = np.array([k for _, k in picks])
+    cols = layout.row_offset[P] + K
+    x = np.stack([datagen.sample_host(np.full(len(cols), r), cols, BF16, NORMAL, seed, sigma) for r in range(world)])
+    want = oracle.reduce_rows(x, pre_div=True)
+    for r in range(world):
+        sel = [i for i, p in enumerate(P) if om["owner"][p] == r or
+               (om["owner"][p] < 0 and om["holder_lo"][p] <= r <= om["holder_hi"][p])]
+        idx = torch.tensor([ex.grad.slot[r][int(P[i])] + int(K[i]) for i in sel], device="cuda")
+        got = to_bits(ex.grad.buf[r][idx])
+        assert np.array_equal(got, want[sel]), f"rank {r}"
+    # probe totals
+    assert sum(p.owner_elems for p in probes) == 295_798_784
+    assert sum(p.reduced_elems for p in probes) == tree.total

@@ -1,0 +1,397 @@
+"""Python binding of libdpred (argument marshalling only).
+
+Every function here forwards to the C-ABI entry point of the same name in
+``libdpred.so`` (declared in ``include/dpred.h``); all device work runs in that
+library's CUDA kernels.  There is no fallback: if the library is missing or a
+call fails, a ``DpredError`` is raised.  PyTorch is used only for device
+memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdpred.so")
+
+BF16, F32 = 0, 1
+MAX_WORLD = 64
+DTYPE_NAMES = {BF16: "BFloat16", F32: "Float"}  # names the probe line prints
+
+# dpred_task: {int32 param_id, int32 reserved, int64 offset, int64 numel}
+TASK_DTYPE = np.dtype([("param_id", "<i4"), ("pad", "<i4"), ("offset", "<i8"), ("numel", "<i8")])
+
+E_CODES = {-1: "DPRED_E_INVAL", -2: "DPRED_E_ALIGN", -3: "DPRED_E_SIZE", -4: "DPRED_E_MISMATCH",
+           -5: "DPRED_E_CUDA", -6: "DPRED_E_TIMEOUT"}
+
+
+class DpredError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{E_CODES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class _Group(ctypes.Structure):
+    _fields_ = [("comm_size", ctypes.c_int32), ("n_params", ctypes.c_int32),
+                ("comm_ranks", ctypes.c_void_p), ("numel", ctypes.c_void_p)]
+
+
+class _Probe(ctypes.Structure):
+    _fields_ = [("flush_index", ctypes.c_int64), ("tasks", ctypes.c_int64), ("reduced_elems", ctypes.c_int64),
+                ("owner_tasks", ctypes.c_int64), ("owner_elems", ctypes.c_int64),
+                ("kept_elems", ctypes.c_int64 * MAX_WORLD)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libdpred.so; raises ImportError when it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                              "(there is no fallback path)")
+        L = ctypes.CDLL(LIB_PATH)
+        i32, i64, vp, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
+        L.dpred_last_error.restype = ctypes.c_char_p
+        L.dpred_version.restype = ctypes.c_char_p
+        L.dpred_build_owner_map.argtypes = [i32, i32, vp, i32, i32, vp, vp, vp, vp, vp]
+        L.dpred_flush_probe.argtypes = [i32, vp, i32, vp, i32, vp, i32, vp]
+        L.dpred_flush_workspace_bytes.restype = ctypes.c_size_t
+        L.dpred_flush_workspace_bytes.argtypes = [i32, i32]
+        L.dpred_flush_bucket.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp, vp,
+                                         ctypes.c_size_t, vp]
+        L.dpred_accumulate_microbatch.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp, vp]
+        L.dpred_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32, vp]
+        L.dpred_allgather.argtypes = [i32, i64, i32, vp, vp, i32, vp]
+        L.dpred_device_status.argtypes = [vp, i32]
+        _lib = L
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise DpredError(rc, lib().dpred_last_error().decode())
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def version() -> str:
+    return lib().dpred_version().decode()
+
+
+# -------------------------------------------------------------- owner map ---
+
+@dataclass
+class OwnerMap:
+    owner: np.ndarray      # int32 per parameter, -1 = AllReduce
+    holder_lo: np.ndarray  # int32
+    holder_hi: np.ndarray  # int32
+    n_owned: int
+    n_total: int
+
+    def report(self) -> str:
+        """The init-time ratio report of the DeepSpeed issue (section "Additional context")."""
+        return f"DeepCompile reduce_to_owner: {self.n_owned}/{self.n_total} gradients reduce to one rank"
+
+
+def build_owner_map(world: int, groups, reduce_to_owner: bool = True, rank: int = 0) -> OwnerMap:
+    """groups: list of (comm_ranks or None, numel sequence) in group order."""
+    keep = []
+    arr = (_Group * max(len(groups), 1))()
+    total = 0
+    for i, (ranks, numel) in enumerate(groups):
+        n = np.ascontiguousarray(numel, dtype=np.int64)
+        keep.append(n)
+        arr[i].n_params = len(n)
+        arr[i].numel = n.ctypes.data if len(n) else None
+        if ranks is None:
+            arr[i].comm_size = world
+            arr[i].comm_ranks = None
+        else:
+            r = np.ascontiguousarray(ranks, dtype=np.int32)
+            keep.append(r)
+            arr[i].comm_size = len(r)
+            arr[i].comm_ranks = r.ctypes.data
+        total += len(n)
+    owner = np.empty(total, np.int32)
+    lo = np.empty(total, np.int32)
+    hi = np.empty(total, np.int32)
+    n_owned, n_total = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().dpred_build_owner_map(world, rank, arr, len(groups), int(reduce_to_owner), owner.ctypes.data,
+                                       lo.ctypes.data, hi.ctypes.data, ctypes.byref(n_owned), ctypes.byref(n_total)))
+    return OwnerMap(owner, lo, hi, n_owned.value, n_total.value)
+
+
+# ------------------------------------------------------------------ probe ---
+
+@dataclass
+class Probe:
+    flush_index: int
+    tasks: int
+    reduced_elems: int
+    owner_tasks: int
+    owner_elems: int
+    kept_elems: list
+
+    def line(self, rank: int, dtype: int, pre_div: bool) -> str:
+        """The probe line of the DeepSpeed issue ("reduce_probe"), for one rank."""
+        red = self.reduced_elems
+        kept = self.kept_elems[rank]
+        disc = 100.0 * (red - kept) / red if red else 0.0
+        own = 100.0 * self.owner_elems / red if red else 0.0
+        return (f"[dc-probe][r{rank}] flushReduceBucket #{self.flush_index} dtype={DTYPE_NAMES[dtype]} "
+                f"tasks={self.tasks} reduced_elems={red} kept_elems={kept} discarded={disc:.1f}% "
+                f"pre_div={int(bool(pre_div))} owner_tasks={self.owner_tasks} owner_elems={self.owner_elems} "
+                f"({own:.1f}%)")
+
+
+class ProbeLog:
+    """Prints one probe line per flush for the first ``limit`` flushes (the
+    issue's reduce_probe prints the first 20)."""
+
+    def __init__(self, rank: int = 0, limit: int = 20, sink=print):
+        self.rank, self.limit, self.sink, self.count = rank, limit, sink, 0
+
+    def next_index(self) -> int:
+        return self.count
+
+    def record(self, probe: Probe, dtype: int, pre_div: bool) -> None:
+        if probe.flush_index < self.limit:
+            self.sink(probe.line(self.rank, dtype, pre_div))
+        self.count += 1
+
+
+def _probe_from(p: _Probe, world: int) -> Probe:
+    return Probe(p.flush_index, p.tasks, p.reduced_elems, p.owner_tasks, p.owner_elems,
+                 [p.kept_elems[r] for r in range(world)])
+
+
+def _tasks_arg(tasks: np.ndarray) -> np.ndarray:
+    t = np.ascontiguousarray(tasks)
+    if t.dtype != TASK_DTYPE:
+        t = np.ascontiguousarray(t.astype(TASK_DTYPE))
+    return t
+
+
+class DstTable:
+    """Host array [world * n_tasks] of destination device pointers (0 = empty
+    buffer), built once and reused across flushes."""
+
+    def __init__(self, world: int, n_tasks: int, ptrs):
+        ptrs = list(ptrs)
+        if len(ptrs) != world * n_tasks:
+            raise ValueError("dst table must have world * n_tasks entries")
+        self.world, self.n_tasks = world, n_tasks
+        self.c = (ctypes.c_void_p * max(len(ptrs), 1))(*[p if p else None for p in ptrs])
+
+    def nonempty(self) -> np.ndarray:
+        return np.array([bool(self.c[i]) for i in range(self.world * self.n_tasks)]).reshape(self.world, self.n_tasks)
+
+
+def flush_probe(world: int, tasks: np.ndarray, owner, dst: DstTable | None, reduce_to_owner: bool = True,
+                flush_index: int = 0) -> Probe:
+    t = _tasks_arg(tasks)
+    own = None if owner is None else np.ascontiguousarray(owner, dtype=np.int32)
+    p = _Probe()
+    p.flush_index = flush_index
+    _check(lib().dpred_flush_probe(world, t.ctypes.data, len(t), None if own is None else own.ctypes.data,
+                                   0 if own is None else len(own), None if dst is None else dst.c,
+                                   int(reduce_to_owner), ctypes.byref(p)))
+    return _probe_from(p, world)
+
+
+def flush_workspace_bytes(world: int, n_tasks: int) -> int:
+    return int(lib().dpred_flush_workspace_bytes(world, n_tasks))
+
+
+def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
+                 pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False, probe: bool = False,
+                 flush_index: int = 0, workspace=None, stream=None):
+    """grads: CUDA tensor [W, m] (row stride = ld, e.g. a column slice of the
+    whole [W, n] gradient); tasks: TASK_DTYPE array; owner: int32 per param or
+    None; dst: DstTable or None (in place).  Returns a Probe when probe=True."""
+    if grads.dim() != 2 or grads.stride(1) != 1:
+        raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
+    world = grads.shape[0]
+    in_dt = _dtype_code(grads)
+    out_dt = in_dt if out_dtype is None else out_dtype
+    ld = grads.stride(0) if world > 1 else grads.shape[1]
+    t = _tasks_arg(tasks)
+    own = None if owner is None else np.ascontiguousarray(owner, dtype=np.int32)
+    p = _Probe() if probe else None
+    if p is not None:
+        p.flush_index = flush_index
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                             workspace.numel() * workspace.element_size())
+    _check(lib().dpred_flush_bucket(world, in_dt, grads.data_ptr(), ld, t.ctypes.data, len(t),
+                                    None if own is None else own.ctypes.data, 0 if own is None else len(own),
+                                    out_dt, None if dst is None else dst.c, int(pre_div), int(reduce_to_owner),
+                                    int(checked), None if p is None else ctypes.byref(p), ws_ptr, ws_bytes,
+                                    _stream(stream)))
+    return _probe_from(p, world) if p is not None else None
+
+
+# ----------------------------------------------------- accumulate / RS / AG ---
+
+def accumulate_microbatch(acc, g, first: bool, finalize: bool, scale: float = 1.0, total=None, stream=None):
+    """acc: fp32 CUDA tensor [W, n]; g: [W, n] bf16/fp32; total: fp32 [n] when finalize."""
+    import torch
+    if acc.dtype != torch.float32 or not acc.is_contiguous() or not g.is_contiguous() or acc.shape != g.shape:
+        raise ValueError("acc must be contiguous fp32 [W, n] and g contiguous [W, n]")
+    if finalize and (total is None or total.dtype != torch.float32 or total.numel() != acc.shape[1]):
+        raise ValueError("finalize needs an fp32 total of n elements")
+    W, n = acc.shape
+    _check(lib().dpred_accumulate_microbatch(W, n, acc.data_ptr(), _dtype_code(g), g.data_ptr(), int(first),
+                                             int(finalize), float(scale),
+                                             total.data_ptr() if finalize else None, _stream(stream)))
+    return total
+
+
+def reduce_scatter(inp, out, pre_div: bool = False, stream=None):
+    """inp: CUDA tensor [N, M]; out: [N, M/N] (bf16 or fp32)."""
+    if not inp.is_contiguous() or not out.is_contiguous():
+        raise ValueError("contiguous tensors required")
+    N, M = inp.shape
+    _check(lib().dpred_reduce_scatter(N, M, _dtype_code(inp), inp.data_ptr(), _dtype_code(out), out.data_ptr(),
+                                      int(pre_div), _stream(stream)))
+    return out
+
+
+def allgather(inp, out, order: int = 0, stream=None):
+    """inp: CUDA tensor [N, S]; out: [N, N*S] of the same dtype; order 0 canonical, 1 ring."""
+    if not inp.is_contiguous() or not out.is_contiguous() or inp.dtype != out.dtype:
+        raise ValueError("contiguous tensors of one dtype required")
+    N, S = inp.shape
+    if tuple(out.shape) != (N, N * S):
+        raise ValueError("out must be [N, N*S]")
+    _check(lib().dpred_allgather(N, S, _dtype_code(inp), inp.data_ptr(), out.data_ptr(), int(order),
+                                 _stream(stream)))
+    return out
+
+
+def device_status(clear: bool = False) -> int:
+    code = ctypes.c_int32()
+    _check(lib().dpred_device_status(ctypes.byref(code), int(clear)))
+    return code.value
+
+
+# ------------------------------------------------------- gradient buffers ---
+
+class GradBuffers:
+    """Real gradient buffers on the ranks that hold a parameter, nothing on the
+    others (the DeepSpeed issue: a real buffer only on the rank whose optimizer
+    partition holds the parameter, ``torch.empty([0])`` everywhere else; a
+    straddling parameter is held by every rank of its partition range).
+
+    One flat CUDA tensor per rank; each held parameter gets a slot whose start
+    keeps the parameter's offset in the gradient row modulo 16 bytes, so the
+    flush can use 16-byte vectors for it."""
+
+    def __init__(self, world: int, omap: OwnerMap, numel, row_offset, dtype, device="cuda", fill=None):
+        import torch
+        self.world = world
+        esize = 2 if dtype == torch.bfloat16 else 4
+        per = 16 // esize
+        numel = np.asarray(numel, dtype=np.int64)
+        row_offset = np.asarray(row_offset, dtype=np.int64)
+        self.slot = [dict() for _ in range(world)]
+        sizes = [0] * world
+        for p in range(len(numel)):
+            lo, hi = int(omap.holder_lo[p]), int(omap.holder_hi[p])
+            if lo < 0 or numel[p] == 0:
+                continue
+            for r in range(lo, hi + 1):
+                start = sizes[r]
+                start += (int(row_offset[p]) - start) % per  # co-align with the gradient row
+                self.slot[r][p] = start
+                sizes[r] = start + int(numel[p])
+        self.buf = []
+        for r in range(world):
+            t = torch.empty(max(sizes[r], 1), dtype=dtype, device=device)
+            if fill is not None:
+                t.fill_(fill)
+            self.buf.append(t)
+        self.numel = numel
+        self.esize = esize
+
+    def view(self, rank: int, param: int):
+        """Rank ``rank``'s buffer for ``param`` (None when it holds none)."""
+        s = self.slot[rank].get(param)
+        if s is None:
+            return None
+        return self.buf[rank][s:s + int(self.numel[param])]
+
+    def dst_table(self, tasks: np.ndarray) -> DstTable:
+        n = len(tasks)
+        ptrs = [0] * (self.world * n)
+        for t, task in enumerate(tasks):
+            p = int(task["param_id"])
+            for r in range(self.world):
+                s = self.slot[r].get(p)
+                if s is not None:
+                    ptrs[r * n + t] = self.buf[r].data_ptr() + s * self.esize
+        return DstTable(self.world, n, ptrs)
+
+
+# ------------------------------------------------------- ZeRO-1 executor ---
+
+class Zero1Executor:
+    """Host runtime of the ZeRO-1 bucket flush on one GPU: the owner map, the
+    installed gradient buffers and one prebuilt destination table per bucket;
+    ``flush_all`` issues one dpred_flush_bucket per bucket on a stream (the
+    DeepSpeed issue's Z1CustomOpExecutor::flushReduceBucket, with the
+    collective replaced by the single-GPU kernel).
+
+    buckets: list of (start, tasks) -- the bucket's element offset in the
+    arrival-order gradient row and its TASK_DTYPE task table."""
+
+    def __init__(self, world: int, numel, row_offset, buckets, dtype, reduce_to_owner: bool = True,
+                 pre_div: bool = True, groups=None, probe_log: ProbeLog | None = None, fill=None):
+        import torch
+        self.world = world
+        self.dtype = dtype
+        self.dt_code = BF16 if dtype == torch.bfloat16 else F32
+        self.reduce_to_owner, self.pre_div = reduce_to_owner, pre_div
+        groups = [(None, numel)] if groups is None else groups
+        self.omap = build_owner_map(world, groups, reduce_to_owner)
+        self.grad = GradBuffers(world, self.omap, numel, row_offset, dtype, fill=fill)
+        self.buckets = [(int(s), np.ascontiguousarray(t, dtype=TASK_DTYPE)) for s, t in buckets]
+        self.tables = [self.grad.dst_table(t) for _, t in self.buckets]
+        self.sizes = [int((t["offset"] + t["numel"]).max()) if len(t) else 0 for _, t in self.buckets]
+        self.probe_log = probe_log
+        ws = max((flush_workspace_bytes(world, len(t)) for _, t in self.buckets), default=0)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda") if ws else None
+
+    def flush_all(self, grads, stream=None, probe: bool = False):
+        """grads: CUDA tensor [W, n] (arrival-order rows).  Returns the probes when probe=True."""
+        probes = []
+        want = probe or self.probe_log is not None
+        for (start, tasks), size, table in zip(self.buckets, self.sizes, self.tables):
+            idx = self.probe_log.next_index() if self.probe_log is not None else len(probes)
+            p = flush_bucket(grads[:, start:start + size], tasks, self.omap.owner, table, self.dt_code,
+                             self.pre_div, self.reduce_to_owner, probe=want, flush_index=idx,
+                             workspace=self.workspace, stream=stream)
+            if self.probe_log is not None:
+                self.probe_log.record(p, self.dt_code, self.pre_div)
+            if probe:
+                probes.append(p)
+        return probes if probe else None

@@ -1,0 +1,352 @@
+// abi.cu -- the extern "C" entry points of libdpred: argument validation, the
+// owner map and probe counters (host metadata), and the flush plan that the
+// kernels execute.  Every entry point validates everything before enqueuing
+// any device work and reports failures as DPRED_E_* codes, never by aborting.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+
+namespace dpred {
+
+__device__ int g_device_error;  // first device-side failure code, 0 when none
+
+namespace {
+thread_local std::string t_last_error;
+
+int elem_size(int dt) { return dt == DPRED_BF16 ? 2 : 4; }
+bool dtype_ok(int dt) { return dt == DPRED_BF16 || dt == DPRED_F32; }
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+bool pow2(int w) { return w > 0 && (w & (w - 1)) == 0; }
+
+struct Dest {
+    int64_t src_off, numel;
+    std::vector<void*> ptrs;  // delivered, non-empty destinations (element 0 of the task)
+};
+
+// Turn per-task destination lists into the kernel plan and launch it.  Tasks
+// with no destination write nothing and are left out of the plan.
+int run_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, int pre_div,
+             const std::vector<Dest>& tasks, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    const int vec_elems = in_dt == DPRED_BF16 ? 8 : 4;
+    const int isz = elem_size(in_dt), osz = elem_size(out_dt);
+    const size_t out_align = std::min<size_t>(16, (size_t)vec_elems * osz);
+    const bool rows_vec = aligned(grads, 16) && (ld * isz) % 16 == 0;
+    std::vector<TaskDesc> plan;
+    std::vector<void*> pool;
+    plan.reserve(tasks.size());
+    int64_t units = 0;
+    for (const Dest& d : tasks) {
+        if (d.numel == 0 || d.ptrs.empty()) continue;
+        TaskDesc t{};
+        t.src_off = d.src_off;
+        t.numel = d.numel;
+        t.dst_begin = (int32_t)pool.size();
+        t.ndst = (int16_t)d.ptrs.size();
+        int64_t head = (vec_elems - d.src_off % vec_elems) % vec_elems;
+        if (head > d.numel) head = d.numel;
+        bool vec = rows_vec;
+        for (void* p : d.ptrs)
+            if ((reinterpret_cast<uintptr_t>(p) + (uintptr_t)head * osz) % out_align != 0) vec = false;
+        t.vec = vec ? 1 : 0;
+        t.head = vec ? (uint8_t)head : 0;
+        t.unit_begin = units;
+        units += flush_task_units(t, vec_elems);
+        pool.insert(pool.end(), d.ptrs.begin(), d.ptrs.end());
+        plan.push_back(t);
+    }
+    if (plan.empty()) return DPRED_OK;
+    FlushLaunch L{};
+    L.h.grads = grads;
+    L.h.ld = ld;
+    L.h.total_units = units;
+    L.h.world = world;
+    L.h.n_tasks = (int32_t)plan.size();
+    L.h.pdiv = (pre_div && world > 1) ? (pow2(world) ? PDIV_POW2 : PDIV_DIV) : PDIV_NONE;
+    L.h.wf = (float)world;
+    L.h.inv_w = 1.0f / (float)world;
+    L.in_dt = in_dt;
+    L.out_dt = out_dt;
+    L.tasks = plan.data();
+    L.dst = pool.data();
+    L.n_dst = (int)pool.size();
+    L.workspace = workspace;
+    L.workspace_bytes = workspace_bytes;
+    return in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
+}
+
+}  // namespace
+
+int set_error(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return code;
+}
+
+int cuda_error(cudaError_t e, const char* what) {
+    return set_error(DPRED_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+int* device_error_word() {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    return static_cast<int*>(p);
+}
+
+}  // namespace dpred
+
+using namespace dpred;
+
+extern "C" {
+
+const char* dpred_last_error(void) { return t_last_error.c_str(); }
+
+const char* dpred_version(void) { return "dpred 0.1 (sm_103a)"; }
+
+int dpred_build_owner_map(int32_t world, int32_t rank, const dpred_group* groups, int32_t n_groups,
+                          int32_t reduce_to_owner, int32_t* owner, int32_t* holder_lo, int32_t* holder_hi,
+                          int32_t* n_owned, int32_t* n_total) {
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (rank < 0 || rank >= world) return set_error(DPRED_E_INVAL, "rank %d outside 0..%d", rank, world - 1);
+    if (n_groups < 0 || (n_groups > 0 && groups == nullptr))
+        return set_error(DPRED_E_INVAL, "bad group list");
+    if (!n_owned || !n_total) return set_error(DPRED_E_INVAL, "null count output");
+    int64_t n_all = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        const dpred_group& G = groups[g];
+        if (G.comm_size < 1 || G.n_params < 0 || (G.n_params > 0 && G.numel == nullptr))
+            return set_error(DPRED_E_INVAL, "group %d: bad comm_size / n_params / numel", g);
+        for (int p = 0; p < G.n_params; ++p)
+            if (G.numel[p] < 0) return set_error(DPRED_E_INVAL, "group %d param %d: negative size", g, p);
+        n_all += G.n_params;
+    }
+    if (n_all > 0 && (!owner || !holder_lo || !holder_hi)) return set_error(DPRED_E_INVAL, "null map output");
+    int32_t owned = 0, total = 0;
+    int64_t out = 0;
+    for (int g = 0; g < n_groups; ++g) {
+        const dpred_group& G = groups[g];
+        bool eligible = G.comm_size == world;
+        for (int i = 0; eligible && G.comm_ranks && i < G.comm_size; ++i) eligible = G.comm_ranks[i] == i;
+        int64_t T = 0;
+        for (int p = 0; p < G.n_params; ++p) T += G.numel[p];
+        const int64_t P = (T + G.comm_size - 1) / G.comm_size;
+        int64_t s = 0;
+        for (int p = 0; p < G.n_params; ++p, ++out) {
+            const int64_t n = G.numel[p];
+            if (n == 0) {
+                owner[out] = holder_lo[out] = holder_hi[out] = -1;
+            } else if (!eligible) {
+                owner[out] = -1;
+                holder_lo[out] = 0;
+                holder_hi[out] = world - 1;
+            } else {
+                const int32_t lo = (int32_t)(s / P), hi = (int32_t)((s + n - 1) / P);
+                holder_lo[out] = lo;
+                holder_hi[out] = hi;
+                owner[out] = (reduce_to_owner && lo == hi) ? lo : -1;
+            }
+            owned += owner[out] >= 0;
+            ++total;
+            s += n;
+        }
+    }
+    *n_owned = owned;
+    *n_total = total;
+    return DPRED_OK;
+}
+
+static int validate_tasks(int32_t world, const dpred_task* tasks, int32_t n_tasks, const int32_t* owner,
+                          int32_t n_params, int64_t ld, bool check_ld) {
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (n_tasks < 0 || (n_tasks > 0 && tasks == nullptr)) return set_error(DPRED_E_INVAL, "bad task list");
+    if (owner && n_params < 0) return set_error(DPRED_E_INVAL, "n_params < 0");
+    for (int t = 0; t < n_tasks; ++t) {
+        const dpred_task& k = tasks[t];
+        if (k.reserved != 0) return set_error(DPRED_E_INVAL, "task %d: reserved field must be 0", t);
+        if (k.offset < 0 || k.numel < 0) return set_error(DPRED_E_INVAL, "task %d: negative offset or size", t);
+        if (check_ld && k.offset + k.numel > ld)
+            return set_error(DPRED_E_SIZE, "task %d: [%lld, %lld) outside the row of %lld elements", t,
+                             (long long)k.offset, (long long)(k.offset + k.numel), (long long)ld);
+        if (owner) {
+            if (k.param_id < 0 || k.param_id >= n_params)
+                return set_error(DPRED_E_INVAL, "task %d: param_id %d outside 0..%d", t, k.param_id, n_params - 1);
+            if (owner[k.param_id] < -1 || owner[k.param_id] >= world)
+                return set_error(DPRED_E_INVAL, "owner of param %d is %d, not a rank", k.param_id, owner[k.param_id]);
+        }
+    }
+    return DPRED_OK;
+}
+
+static int root_of(const dpred_task& k, const int32_t* owner, int32_t reduce_to_owner) {
+    return (reduce_to_owner && owner && owner[k.param_id] >= 0) ? owner[k.param_id] : -1;
+}
+
+static void fill_probe(int32_t world, const dpred_task* tasks, int32_t n_tasks, const int32_t* owner,
+                       void* const* dst, int32_t reduce_to_owner, dpred_probe* probe) {
+    probe->tasks = n_tasks;
+    probe->reduced_elems = probe->owner_tasks = probe->owner_elems = 0;
+    for (int r = 0; r < DPRED_MAX_WORLD; ++r) probe->kept_elems[r] = 0;
+    for (int t = 0; t < n_tasks; ++t) {
+        const int root = root_of(tasks[t], owner, reduce_to_owner);
+        probe->reduced_elems += tasks[t].numel;
+        if (root >= 0) {
+            probe->owner_tasks += 1;
+            probe->owner_elems += tasks[t].numel;
+        }
+        for (int r = 0; r < world; ++r) {
+            bool kept = dst ? dst[(int64_t)r * n_tasks + t] != nullptr : (root < 0 || root == r);
+            if (kept) probe->kept_elems[r] += tasks[t].numel;
+        }
+    }
+}
+
+int dpred_flush_probe(int32_t world, const dpred_task* tasks, int32_t n_tasks, const int32_t* owner,
+                      int32_t n_params, void* const* dst, int32_t reduce_to_owner, dpred_probe* probe) {
+    int rc = validate_tasks(world, tasks, n_tasks, owner, n_params, 0, false);
+    if (rc) return rc;
+    if (!probe) return set_error(DPRED_E_INVAL, "null probe");
+    fill_probe(world, tasks, n_tasks, owner, dst, reduce_to_owner, probe);
+    return DPRED_OK;
+}
+
+size_t dpred_flush_workspace_bytes(int32_t world, int32_t n_tasks) {
+    if (world < 1 || n_tasks < 0) return 0;
+    const int64_t dsts = (int64_t)world * n_tasks;
+    if (n_tasks <= kInlineTasks && dsts <= kInlineDst) return 0;
+    return sizeof(TaskDesc) * (size_t)n_tasks + (((size_t)dsts * sizeof(void*) + 15) & ~(size_t)15);
+}
+
+int dpred_flush_bucket(int32_t world, int32_t in_dtype, void* grads, int64_t ld, const dpred_task* tasks,
+                       int32_t n_tasks, const int32_t* owner, int32_t n_params, int32_t out_dtype, void* const* dst,
+                       int32_t pre_div, int32_t reduce_to_owner, int32_t checked, dpred_probe* probe,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    if (ld < 0) return set_error(DPRED_E_INVAL, "ld < 0");
+    int rc = validate_tasks(world, tasks, n_tasks, owner, n_params, ld, true);
+    if (rc) return rc;
+    const int isz = elem_size(in_dtype), osz = elem_size(out_dtype);
+    bool any = false;
+    for (int t = 0; t < n_tasks; ++t) any |= tasks[t].numel > 0;
+    if (any && grads == nullptr) return set_error(DPRED_E_INVAL, "null grads");
+    if (grads && !aligned(grads, isz)) return set_error(DPRED_E_ALIGN, "grads not aligned to its element size");
+    if (dst == nullptr) {
+        if (out_dtype != in_dtype) return set_error(DPRED_E_INVAL, "in-place flush needs out_dtype == in_dtype");
+        std::vector<std::pair<int64_t, int64_t>> r;
+        for (int t = 0; t < n_tasks; ++t)
+            if (tasks[t].numel > 0) r.emplace_back(tasks[t].offset, tasks[t].offset + tasks[t].numel);
+        std::sort(r.begin(), r.end());
+        for (size_t i = 1; i < r.size(); ++i)
+            if (r[i].first < r[i - 1].second) return set_error(DPRED_E_SIZE, "in-place tasks overlap");
+    } else {
+        for (int64_t i = 0; i < (int64_t)world * n_tasks; ++i)
+            if (dst[i] && !aligned(dst[i], osz))
+                return set_error(DPRED_E_ALIGN, "destination %lld not aligned to its element size", (long long)i);
+    }
+    if (checked && dst) {
+        for (int t = 0; t < n_tasks; ++t) {
+            const int root = root_of(tasks[t], owner, reduce_to_owner);
+            if (root < 0) continue;
+            for (int r = 0; r < world; ++r)
+                if (r != root && dst[(int64_t)r * n_tasks + t] != nullptr)
+                    return set_error(DPRED_E_MISMATCH,
+                                     "task %d (param %d) is owned by rank %d but rank %d has a non-empty buffer", t,
+                                     tasks[t].param_id, root, r);
+        }
+    }
+    if (probe) fill_probe(world, tasks, n_tasks, owner, dst, reduce_to_owner, probe);
+
+    std::vector<Dest> plan(n_tasks);
+    for (int t = 0; t < n_tasks; ++t) {
+        const int root = root_of(tasks[t], owner, reduce_to_owner);
+        Dest& d = plan[t];
+        d.src_off = tasks[t].offset;
+        d.numel = tasks[t].numel;
+        for (int r = 0; r < world; ++r) {
+            if (root >= 0 && r != root) continue;  // not delivered: untouched
+            void* p = dst ? dst[(int64_t)r * n_tasks + t]
+                          : static_cast<char*>(grads) + ((int64_t)r * ld + tasks[t].offset) * isz;
+            if (p) d.ptrs.push_back(p);  // empty buffer: skipped in the copy-out
+        }
+    }
+    return run_plan(world, in_dtype, grads, ld, out_dtype, pre_div, plan, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int dpred_accumulate_microbatch(int32_t world, int64_t n, float* acc, int32_t g_dtype, const void* g,
+                                int32_t first, int32_t finalize, float scale, float* total, void* stream) {
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (n < 0) return set_error(DPRED_E_INVAL, "n < 0");
+    if (!dtype_ok(g_dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    if (n > 0 && (!acc || !g || (finalize && !total))) return set_error(DPRED_E_INVAL, "null pointer");
+    if ((acc && !aligned(acc, 4)) || (g && !aligned(g, elem_size(g_dtype))) || (total && !aligned(total, 4)))
+        return set_error(DPRED_E_ALIGN, "pointer not aligned to its element size");
+    return launch_accumulate(world, n, acc, g_dtype, g, first, finalize, scale, total,
+                             static_cast<cudaStream_t>(stream));
+}
+
+int dpred_reduce_scatter(int32_t n_nodes, int64_t m_elems, int32_t in_dtype, const void* in, int32_t out_dtype,
+                         void* out, int32_t pre_div, void* stream) {
+    if (n_nodes < 1 || n_nodes > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "n_nodes %d outside 1..%d", n_nodes, DPRED_MAX_WORLD);
+    if (m_elems < 0) return set_error(DPRED_E_INVAL, "m_elems < 0");
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    if (m_elems % n_nodes != 0) return set_error(DPRED_E_SIZE, "M = %lld is not a multiple of N = %d", (long long)m_elems, n_nodes);
+    if (m_elems > 0 && (!in || !out)) return set_error(DPRED_E_INVAL, "null pointer");
+    if ((in && !aligned(in, elem_size(in_dtype))) || (out && !aligned(out, elem_size(out_dtype))))
+        return set_error(DPRED_E_ALIGN, "pointer not aligned to its element size");
+    const int64_t S = m_elems / n_nodes;
+    std::vector<Dest> plan(n_nodes);
+    for (int i = 0; i < n_nodes; ++i) {
+        plan[i].src_off = (int64_t)i * S;
+        plan[i].numel = S;
+        plan[i].ptrs.push_back(static_cast<char*>(out) + (int64_t)i * S * elem_size(out_dtype));
+    }
+    return run_plan(n_nodes, in_dtype, in, m_elems, out_dtype, pre_div, plan, nullptr, 0,
+                    static_cast<cudaStream_t>(stream));
+}
+
+int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const void* in, void* out, int32_t order,
+                    void* stream) {
+    if (n_nodes < 1 || n_nodes > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "n_nodes %d outside 1..%d", n_nodes, DPRED_MAX_WORLD);
+    if (shard_elems < 0) return set_error(DPRED_E_INVAL, "shard_elems < 0");
+    if (!dtype_ok(dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    if (order != 0 && order != 1) return set_error(DPRED_E_INVAL, "order must be 0 (canonical) or 1 (ring)");
+    if (shard_elems > 0 && (!in || !out)) return set_error(DPRED_E_INVAL, "null pointer");
+    const int esz = elem_size(dtype);
+    if ((in && !aligned(in, esz)) || (out && !aligned(out, esz)))
+        return set_error(DPRED_E_ALIGN, "pointer not aligned to its element size");
+    return launch_allgather(n_nodes, shard_elems, esz, in, out, order, static_cast<cudaStream_t>(stream));
+}
+
+int dpred_device_status(int32_t* code, int32_t clear) {
+    if (!code) return set_error(DPRED_E_INVAL, "null code");
+    cudaError_t e = cudaMemcpyFromSymbol(code, g_device_error, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_error(e, "reading the device error word");
+    if (clear) {
+        int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero);
+        if (e != cudaSuccess) return cuda_error(e, "clearing the device error word");
+    }
+    return DPRED_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,222 @@
+// accumulate.cu -- replica-local gradient accumulation and the one cross-replica
+// reduction per optimizer step.
+//
+// MaxText PR #5099 "Defer the data-parallel gradient all-reduce to update()
+// under gradient accumulation", section "What": cotangents stay per-replica
+// partial sums that accumulate replica-locally across micro-batches, and the
+// single cross-replica all-reduce happens once, in update().  Here the W
+// replica accumulators are rows of one [W, n] fp32 array; a micro-batch adds
+// its [W, n] gradient row by row (acc += g), and the last micro-batch's add is
+// fused with the reduction over rows (total = sum_r (acc_r + g_r)), so the
+// accumulator is read once and never written back on that pass.
+#include "common.cuh"
+
+namespace dpred {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+
+template <typename Tg>
+struct G;
+template <>
+struct G<__nv_bfloat16> {
+    using V = uint2;  // 4 bf16
+    __device__ static void widen(const V& v, float (&f)[4]) {
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    }
+    __device__ static float one(const __nv_bfloat16* p) { return bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(p)); }
+};
+template <>
+struct G<float> {
+    using V = float4;
+    __device__ static void widen(const V& v, float (&f)[4]) { f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w; }
+    __device__ static float one(const float* p) { return *p; }
+};
+
+// acc[i] = first ? g[i] : acc[i] + g[i] over the flat [W * n] range.
+template <typename Tg, bool FIRST>
+__global__ void __launch_bounds__(kThreads) accumulate_kernel(float* __restrict__ acc, const Tg* __restrict__ g,
+                                                              int64_t total, int vec) {
+    using V = typename G<Tg>::V;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nv = total / 4;
+        float4* a4 = reinterpret_cast<float4*>(acc);
+        const V* g4 = reinterpret_cast<const V*>(g);
+        for (int64_t v0 = tid; v0 < nv; v0 += nthreads * kUnroll) {
+            float4 av[kUnroll];
+            V gv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                int64_t v = v0 + u * nthreads;
+                if (v < nv) {
+                    if (!FIRST) av[u] = __ldcs(a4 + v);
+                    gv[u] = __ldcs(g4 + v);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                int64_t v = v0 + u * nthreads;
+                if (v < nv) {
+                    float f[4];
+                    G<Tg>::widen(gv[u], f);
+                    float4 o;
+                    if (FIRST) {
+                        o = make_float4(f[0], f[1], f[2], f[3]);
+                    } else {
+                        o = make_float4(__fadd_rn(av[u].x, f[0]), __fadd_rn(av[u].y, f[1]), __fadd_rn(av[u].z, f[2]),
+                                        __fadd_rn(av[u].w, f[3]));
+                    }
+                    __stcs(a4 + v, o);
+                }
+            }
+        }
+        done = nv * 4;
+    }
+    for (int64_t i = done + tid; i < total; i += nthreads) {
+        float gv = G<Tg>::one(g + i);
+        acc[i] = FIRST ? gv : __fadd_rn(acc[i], gv);
+    }
+}
+
+// total[k] = (sum over r in order of (first ? g[r][k] : acc[r][k] + g[r][k])) * scale.
+template <int W_T, typename Tg, bool FIRST>
+__global__ void __launch_bounds__(kThreads) finalize_kernel(const float* __restrict__ acc, const Tg* __restrict__ g,
+                                                            float* __restrict__ total, int world, int64_t n,
+                                                            float scale, int vec) {
+    using V = typename G<Tg>::V;
+    const int W = W_T > 0 ? W_T : world;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nv = n / 4;
+        const float4* a4 = reinterpret_cast<const float4*>(acc);
+        const V* g4 = reinterpret_cast<const V*>(g);
+        float4* t4 = reinterpret_cast<float4*>(total);
+        for (int64_t v = tid; v < nv; v += nthreads) {
+            float y[4];
+            if constexpr (W_T > 0) {
+                float4 av[W_T];
+                V gv[W_T];
+#pragma unroll
+                for (int r = 0; r < W_T; ++r) {
+                    if (!FIRST) av[r] = __ldcs(a4 + r * nv + v);
+                    gv[r] = __ldcs(g4 + r * nv + v);
+                }
+#pragma unroll
+                for (int r = 0; r < W_T; ++r) {
+                    float f[4];
+                    G<Tg>::widen(gv[r], f);
+                    float a[4] = {f[0], f[1], f[2], f[3]};
+                    if (!FIRST) {
+                        a[0] = __fadd_rn(av[r].x, f[0]); a[1] = __fadd_rn(av[r].y, f[1]);
+                        a[2] = __fadd_rn(av[r].z, f[2]); a[3] = __fadd_rn(av[r].w, f[3]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) y[j] = (r == 0) ? a[j] : __fadd_rn(y[j], a[j]);
+                }
+            } else {
+                for (int r = 0; r < W; ++r) {
+                    float f[4];
+                    G<Tg>::widen(__ldcs(g4 + r * nv + v), f);
+                    if (!FIRST) {
+                        float4 av = __ldcs(a4 + r * nv + v);
+                        f[0] = __fadd_rn(av.x, f[0]); f[1] = __fadd_rn(av.y, f[1]);
+                        f[2] = __fadd_rn(av.z, f[2]); f[3] = __fadd_rn(av.w, f[3]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) y[j] = (r == 0) ? f[j] : __fadd_rn(y[j], f[j]);
+                }
+            }
+            __stcs(t4 + v, make_float4(__fmul_rn(y[0], scale), __fmul_rn(y[1], scale), __fmul_rn(y[2], scale),
+                                       __fmul_rn(y[3], scale)));
+        }
+        done = nv * 4;
+    }
+    for (int64_t k = done + tid; k < n; k += nthreads) {
+        float y = 0.0f;
+        for (int r = 0; r < W; ++r) {
+            float a = G<Tg>::one(g + (int64_t)r * n + k);
+            if (!FIRST) a = __fadd_rn(acc[(int64_t)r * n + k], a);
+            y = (r == 0) ? a : __fadd_rn(y, a);
+        }
+        total[k] = __fmul_rn(y, scale);
+    }
+}
+
+template <typename K>
+unsigned grid_for(K kernel, int64_t work_items) {
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess || occ < 1) occ = 1;
+    int64_t g = (int64_t)sm_count() * occ;
+    int64_t need = (work_items + kThreads - 1) / kThreads;
+    if (need < 1) need = 1;
+    return (unsigned)(need < g ? need : g);
+}
+
+template <typename Tg, bool FIRST>
+int launch_finalize(int world, int64_t n, const float* acc, const Tg* g, float* total, float scale, int vec,
+                    cudaStream_t s) {
+    int64_t items = vec ? n / 4 : n;
+#define DPRED_FIN(WT)                                                                     \
+    {                                                                                     \
+        auto k = finalize_kernel<WT, Tg, FIRST>;                                          \
+        k<<<grid_for(k, items), kThreads, 0, s>>>(acc, g, total, world, n, scale, vec);   \
+        break;                                                                            \
+    }
+    switch (world) {
+        case 1: DPRED_FIN(1)
+        case 2: DPRED_FIN(2)
+        case 4: DPRED_FIN(4)
+        case 8: DPRED_FIN(8)
+        default: DPRED_FIN(0)
+    }
+#undef DPRED_FIN
+    return DPRED_OK;
+}
+
+template <typename Tg>
+int launch_typed(int world, int64_t n, float* acc, const Tg* g, int first, int finalize, float scale, float* total,
+                 cudaStream_t s) {
+    const int64_t total_elems = (int64_t)world * n;
+    const uintptr_t ga = reinterpret_cast<uintptr_t>(g), aa = reinterpret_cast<uintptr_t>(acc);
+    const int gvec = (int)sizeof(typename G<Tg>::V);
+    if (!finalize) {
+        // flat over [W * n]: rows are contiguous, so only the bases need alignment
+        int vec = (aa % 16 == 0) && (ga % gvec == 0);
+        int64_t items = vec ? total_elems / 4 : total_elems;
+        if (first) {
+            auto k = accumulate_kernel<Tg, true>;
+            k<<<grid_for(k, items), kThreads, 0, s>>>(acc, g, total_elems, vec);
+        } else {
+            auto k = accumulate_kernel<Tg, false>;
+            k<<<grid_for(k, items), kThreads, 0, s>>>(acc, g, total_elems, vec);
+        }
+    } else {
+        // per column: every row start must keep the vector alignment
+        int vec = (aa % 16 == 0) && (ga % gvec == 0) && (n % 4 == 0) &&
+                  (reinterpret_cast<uintptr_t>(total) % 16 == 0);
+        if (first)
+            launch_finalize<Tg, true>(world, n, acc, g, total, scale, vec, s);
+        else
+            launch_finalize<Tg, false>(world, n, acc, g, total, scale, vec, s);
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DPRED_OK : cuda_error(e, "accumulate kernel launch");
+}
+
+}  // namespace
+
+int launch_accumulate(int world, int64_t n, float* acc, int g_dt, const void* g, int first, int finalize, float scale,
+                      float* total, cudaStream_t s) {
+    if ((int64_t)world * n == 0) return DPRED_OK;
+    if (g_dt == DPRED_BF16)
+        return launch_typed(world, n, acc, static_cast<const __nv_bfloat16*>(g), first, finalize, scale, total, s);
+    return launch_typed(world, n, acc, static_cast<const float*>(g), first, finalize, scale, total, s);
+}
+
+}  // namespace dpred

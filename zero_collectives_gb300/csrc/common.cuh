@@ -1,0 +1,133 @@
+// common.cuh -- internal declarations shared by the libdpred translation units.
+//
+// Element rule of every reduction in this library (the pages' "same reduction,
+// same operand order per element"): widen each term to fp32, optionally
+// pre-divide it by the number of ranks, add the terms in rank order starting
+// from the rank-0 term, round once to the output type.  Every fp32 operation
+// is written with an explicit round-to-nearest intrinsic so that no compiler
+// contraction (FMA) can change a bit.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dpred.h"
+
+namespace dpred {
+
+// ------------------------------------------------------------------ errors --
+
+int set_error(int code, const char* fmt, ...);
+int cuda_error(cudaError_t e, const char* what);
+
+// ----------------------------------------------------------- device info ---
+
+int sm_count();  // SMs of the current device (cached per device)
+
+// ---------------------------------------------------------- element math ---
+
+// Pre-division modes: none, multiply by the exact reciprocal of a power-of-two
+// rank count (bit-identical to dividing), IEEE division by any rank count.
+enum PreDiv : int { PDIV_NONE = 0, PDIV_POW2 = 1, PDIV_DIV = 2 };
+
+__device__ __forceinline__ float pre_divide(float x, int mode, float wf, float inv_w) {
+    if (mode == PDIV_POW2) return __fmul_rn(x, inv_w);
+    if (mode == PDIV_DIV) return __fdiv_rn(x, wf);
+    return x;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 values to a bf16x2 word (round to nearest even); `lo` goes to the
+// low half, i.e. the lower address.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&v);
+}
+
+// ------------------------------------------------------------ flush plan ---
+
+// One task of a flush as the kernel sees it (built on the host).
+struct TaskDesc {
+    int64_t src_off;     // element offset of the task in every row
+    int64_t numel;       // elements (> 0)
+    int64_t unit_begin;  // first work unit of the task (prefix over the plan)
+    int32_t dst_begin;   // first destination pointer in the plan's pointer pool
+    int16_t ndst;        // destinations to write (0..world)
+    uint8_t vec;         // 1: 16-byte vector path (rows and destinations co-aligned)
+    uint8_t head;        // scalar elements before the first 16-byte aligned vector
+};
+static_assert(sizeof(TaskDesc) == 32, "TaskDesc layout");
+
+struct FlushHeader {
+    const void* grads;
+    int64_t ld;          // row stride in elements
+    int64_t total_units;
+    int32_t world;
+    int32_t n_tasks;
+    int32_t pdiv;        // PreDiv
+    float wf, inv_w;     // world as float, its reciprocal (exact for powers of two)
+};
+
+constexpr int kInlineTasks = 128;
+constexpr int kInlineDst = 512;
+
+// Plan carried inside the launch (kernel parameter space, read through the
+// constant cache): no device workspace and no host-to-device copy.
+struct FlushArgsInline {
+    FlushHeader h;
+    TaskDesc tasks[kInlineTasks];
+    void* dst[kInlineDst];
+};
+
+// Plan in caller-provided device workspace.
+struct FlushArgsWs {
+    FlushHeader h;
+    const TaskDesc* tasks;
+    void* const* dst;
+};
+
+constexpr int kFlushThreads = 256;
+constexpr int kUnitVec = 1024;     // 16-byte vectors per work unit of the vector path
+constexpr int kUnitScalar = 2048;  // elements per work unit of the scalar path
+
+struct FlushLaunch {
+    FlushHeader h;
+    int in_dt, out_dt;
+    const TaskDesc* tasks;   // host plan
+    void* const* dst;        // host pointer pool
+    int n_dst;
+    void* workspace;         // device, used when the plan does not fit inline
+    size_t workspace_bytes;
+};
+
+// Work units of a plan task; vec_elems = input elements per 16-byte vector.
+inline int64_t flush_task_units(const TaskDesc& t, int vec_elems) {
+    if (t.vec) {
+        int64_t nbody = (t.numel - t.head) / vec_elems;
+        int64_t u = (nbody + kUnitVec - 1) / kUnitVec;
+        return u > 0 ? u : 1;
+    }
+    return (t.numel + kUnitScalar - 1) / kUnitScalar;
+}
+
+int launch_flush_bf16_in(const FlushLaunch& L, cudaStream_t s);
+int launch_flush_f32_in(const FlushLaunch& L, cudaStream_t s);
+
+int launch_accumulate(int world, int64_t n, float* acc, int g_dt, const void* g, int first, int finalize,
+                      float scale, float* total, cudaStream_t s);
+
+int launch_allgather(int n_nodes, int64_t shard_elems, int esize, const void* in, void* out, int order,
+                     cudaStream_t s);
+
+int* device_error_word();  // device address of the error word (current device)
+
+}  // namespace dpred

@@ -1,0 +1,269 @@
+// flush_kernels.cuh -- the bucket-flush kernel (reduce to owner / AllReduce
+// fallback / empty-buffer skip), shared by ReduceScatter.
+//
+// DeepSpeed issue #8700 "[REQUEST] DeepCompile ZeRO-1: reduce-to-owner instead
+// of AllReduce": each bucket task is one whole parameter; its reduced value
+// goes to the owner's buffer only (ncclReduce(root=owner)) or, for a parameter
+// straddling a partition boundary, to every rank's buffer (ncclAllReduce), and
+// empty buffers are skipped in the copy-out.  On one GPU the W replicas are W
+// rows of the bucket, so the "collective" is a streaming reduction over the
+// rows whose store goes straight into the delivered, non-empty destinations:
+// the copy-out is fused into the store.
+//
+// Work decomposition: the host cuts every task into work units (1024 16-byte
+// vectors on the vector path, 2048 elements on the scalar path); a persistent
+// grid strides over units in bucket order and finds each unit's task by a
+// binary search over the plan (all threads of a CTA read the same entries, a
+// broadcast from the constant cache).  Each thread keeps W x BATCH 16-byte
+// loads in flight, then reduces them in rank order.
+#pragma once
+
+#include "common.cuh"
+
+namespace dpred {
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;  // elements per 16-byte vector
+    __device__ static float load(const __nv_bfloat16* p) {
+        return bf16_bits_to_f32(*reinterpret_cast<const uint16_t*>(p));
+    }
+    __device__ static void store(__nv_bfloat16* p, float v) { *reinterpret_cast<uint16_t*>(p) = f32_to_bf16_bits(v); }
+};
+template <>
+struct Elem<float> {
+    static constexpr int kVec = 4;
+    __device__ static float load(const float* p) { return *p; }
+    __device__ static void store(float* p, float v) { *p = v; }
+};
+
+__device__ __forceinline__ const TaskDesc& plan_task(const FlushArgsInline& a, int i) { return a.tasks[i]; }
+__device__ __forceinline__ const TaskDesc& plan_task(const FlushArgsWs& a, int i) { return a.tasks[i]; }
+__device__ __forceinline__ void* plan_dst(const FlushArgsInline& a, int i) { return a.dst[i]; }
+__device__ __forceinline__ void* plan_dst(const FlushArgsWs& a, int i) { return a.dst[i]; }
+
+// Unpack one 16-byte input vector into fp32 values.
+template <typename Tin>
+__device__ __forceinline__ void unpack(const uint4& q, float (&f)[Elem<Tin>::kVec]);
+template <>
+__device__ __forceinline__ void unpack<__nv_bfloat16>(const uint4& q, float (&f)[8]) {
+    f[0] = bf16_lo(q.x); f[1] = bf16_hi(q.x);
+    f[2] = bf16_lo(q.y); f[3] = bf16_hi(q.y);
+    f[4] = bf16_lo(q.z); f[5] = bf16_hi(q.z);
+    f[6] = bf16_lo(q.w); f[7] = bf16_hi(q.w);
+}
+template <>
+__device__ __forceinline__ void unpack<float>(const uint4& q, float (&f)[4]) {
+    f[0] = __uint_as_float(q.x); f[1] = __uint_as_float(q.y);
+    f[2] = __uint_as_float(q.z); f[3] = __uint_as_float(q.w);
+}
+
+// Store VEC reduced values (already rounded in the caller's order) to dst.
+template <typename Tout, int VEC>
+__device__ __forceinline__ void store_vec(Tout* p, const float (&y)[VEC]);
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16, 8>(__nv_bfloat16* p, const float (&y)[8]) {
+    uint4 q = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                         pack_bf16x2(y[6], y[7]));
+    __stcs(reinterpret_cast<uint4*>(p), q);
+}
+template <>
+__device__ __forceinline__ void store_vec<__nv_bfloat16, 4>(__nv_bfloat16* p, const float (&y)[4]) {
+    uint2 q = make_uint2(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]));
+    __stcs(reinterpret_cast<uint2*>(p), q);
+}
+template <>
+__device__ __forceinline__ void store_vec<float, 8>(float* p, const float (&y)[8]) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
+    __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(y[4], y[5], y[6], y[7]));
+}
+template <>
+__device__ __forceinline__ void store_vec<float, 4>(float* p, const float (&y)[4]) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
+}
+
+// Fold one replica's vector into the running sums (rank order is the call order).
+template <typename Tin, int MODE>
+__device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q, bool first, float wf, float inv_w) {
+    constexpr int VEC = Elem<Tin>::kVec;
+    float f[VEC];
+    unpack<Tin>(q, f);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        float t = pre_divide(f[j], MODE, wf, inv_w);
+        y[j] = first ? t : __fadd_rn(y[j], t);
+    }
+}
+
+// One element on the scalar path (heads, tails, tasks that are not co-aligned).
+template <typename Tin, typename Tout, int MODE, typename Args>
+__device__ void flush_element(const Args& a, const TaskDesc& T, int64_t k) {
+    const FlushHeader& h = a.h;
+    const Tin* x = static_cast<const Tin*>(h.grads) + T.src_off + k;
+    float y = 0.0f;
+    for (int r = 0; r < h.world; ++r) {
+        float t = pre_divide(Elem<Tin>::load(x + (int64_t)r * h.ld), MODE, h.wf, h.inv_w);
+        y = (r == 0) ? t : __fadd_rn(y, t);
+    }
+    for (int d = 0; d < T.ndst; ++d) Elem<Tout>::store(static_cast<Tout*>(plan_dst(a, T.dst_begin + d)) + k, y);
+}
+
+// Vector body of one work unit: vectors [v0, v1) of the task's aligned body.
+template <int W_T, int BATCH, typename Tin, typename Tout, int MODE, typename Args>
+__device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T, int64_t v0, int64_t v1) {
+    constexpr int VEC = Elem<Tin>::kVec;
+    const FlushHeader& h = a.h;
+    const int64_t stride = h.ld / VEC;  // row stride in vectors
+    const uint4* base = reinterpret_cast<const uint4*>(static_cast<const Tin*>(h.grads) + T.src_off + T.head);
+    for (int64_t vb = v0 + threadIdx.x; vb < v1; vb += (int64_t)kFlushThreads * BATCH) {
+        float y[BATCH][VEC];
+        if constexpr (W_T > 0) {
+            uint4 q[W_T][BATCH];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                int64_t v = vb + (int64_t)b * kFlushThreads;
+                if (v < v1) {
+#pragma unroll
+                    for (int r = 0; r < W_T; ++r) q[r][b] = __ldcs(base + r * stride + v);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                if (vb + (int64_t)b * kFlushThreads < v1) {
+#pragma unroll
+                    for (int r = 0; r < W_T; ++r) fold<Tin, MODE>(y[b], q[r][b], r == 0, h.wf, h.inv_w);
+                }
+            }
+        } else {
+            // Any world size: rows in chunks of 8 loads in flight, folded in rank order.
+            static_assert(BATCH == 1, "generic path keeps one vector per thread");
+            int64_t v = vb;
+            for (int r0 = 0; r0 < h.world; r0 += 8) {
+                uint4 q[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r0 + r < h.world) q[r] = __ldcs(base + (int64_t)(r0 + r) * stride + v);
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+                    if (r0 + r < h.world) fold<Tin, MODE>(y[0], q[r], r0 + r == 0, h.wf, h.inv_w);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            int64_t v = vb + (int64_t)b * kFlushThreads;
+            if (v < v1) {
+                int64_t e = T.head + v * VEC;  // element index inside the task
+                for (int d = 0; d < T.ndst; ++d)
+                    store_vec<Tout, VEC>(static_cast<Tout*>(plan_dst(a, T.dst_begin + d)) + e, y[b]);
+            }
+        }
+    }
+}
+
+template <int W_T, int BATCH, typename Tin, typename Tout, int MODE, typename Args>
+__device__ __forceinline__ void flush_unit(const Args& a, const TaskDesc& T, int64_t local) {
+    constexpr int VEC = Elem<Tin>::kVec;
+    if (T.vec) {
+        const int64_t nbody = (T.numel - T.head) / VEC;
+        const int64_t v0 = local * kUnitVec;
+        const int64_t v1 = v0 + kUnitVec < nbody ? v0 + kUnitVec : nbody;
+        flush_unit_vec<W_T, BATCH, Tin, Tout, MODE>(a, T, v0, v1);
+        if (local == 0) {
+            const int tail = (int)(T.numel - T.head - nbody * VEC);
+            const int id = threadIdx.x;
+            if (id < T.head)
+                flush_element<Tin, Tout, MODE>(a, T, id);
+            else if (id < T.head + tail)
+                flush_element<Tin, Tout, MODE>(a, T, T.head + nbody * VEC + (id - T.head));
+        }
+    } else {
+        const int64_t e0 = local * kUnitScalar;
+        const int64_t e1 = e0 + kUnitScalar < T.numel ? e0 + kUnitScalar : T.numel;
+        for (int64_t k = e0 + threadIdx.x; k < e1; k += kFlushThreads) flush_element<Tin, Tout, MODE>(a, T, k);
+    }
+}
+
+template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
+__global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_constant__ Args a) {
+    const FlushHeader& h = a.h;
+    for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
+        int lo = 0, hi = h.n_tasks - 1;  // last task with unit_begin <= u
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if (plan_task(a, mid).unit_begin <= u)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const TaskDesc T = plan_task(a, lo);
+        const int64_t local = u - T.unit_begin;
+        if (h.pdiv == PDIV_POW2)
+            flush_unit<W_T, BATCH, Tin, Tout, PDIV_POW2>(a, T, local);
+        else if (h.pdiv == PDIV_DIV)
+            flush_unit<W_T, BATCH, Tin, Tout, PDIV_DIV>(a, T, local);
+        else
+            flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE>(a, T, local);
+    }
+}
+
+// Persistent grid: SMs x resident CTAs (queried once per kernel), capped by the number of units.
+template <typename K>
+int64_t persistent_grid(K kernel, int64_t units) {
+    static int occ = 0;
+    if (occ == 0) {
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kFlushThreads, 0) != cudaSuccess || o < 1) o = 1;
+        occ = o;
+    }
+    int64_t g = (int64_t)sm_count() * occ;
+    return units < g ? units : g;
+}
+
+template <int W_T, int BATCH, typename Tin, typename Tout>
+int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
+    const FlushHeader& h = L.h;
+    if (h.total_units == 0) return DPRED_OK;
+    if (h.n_tasks <= kInlineTasks && L.n_dst <= kInlineDst) {
+        FlushArgsInline a;
+        a.h = h;
+        for (int i = 0; i < h.n_tasks; ++i) a.tasks[i] = L.tasks[i];
+        for (int i = 0; i < L.n_dst; ++i) a.dst[i] = L.dst[i];
+        auto k = flush_kernel<W_T, BATCH, Tin, Tout, FlushArgsInline>;
+        k<<<(unsigned)persistent_grid(k, h.total_units), kFlushThreads, 0, s>>>(a);
+    } else {
+        size_t tb = sizeof(TaskDesc) * (size_t)h.n_tasks, db = sizeof(void*) * (size_t)L.n_dst;
+        size_t need = tb + ((db + 15) & ~(size_t)15);
+        if (L.workspace == nullptr || L.workspace_bytes < need)
+            return set_error(DPRED_E_SIZE, "flush plan of %d tasks / %d destinations needs %zu bytes of workspace, got %zu",
+                             h.n_tasks, L.n_dst, need, L.workspace_bytes);
+        if ((reinterpret_cast<uintptr_t>(L.workspace) & 15) != 0)
+            return set_error(DPRED_E_ALIGN, "flush workspace must be 16-byte aligned");
+        char* ws = static_cast<char*>(L.workspace);
+        cudaError_t e = cudaMemcpyAsync(ws, L.tasks, tb, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess && db) e = cudaMemcpyAsync(ws + tb, L.dst, db, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_error(e, "flush plan copy");
+        FlushArgsWs a;
+        a.h = h;
+        a.tasks = reinterpret_cast<const TaskDesc*>(ws);
+        a.dst = reinterpret_cast<void* const*>(ws + tb);
+        auto k = flush_kernel<W_T, BATCH, Tin, Tout, FlushArgsWs>;
+        k<<<(unsigned)persistent_grid(k, h.total_units), kFlushThreads, 0, s>>>(a);
+    }
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
+}
+
+template <typename Tin, typename Tout>
+int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
+    switch (L.h.world) {
+        case 2: return launch_flush_w<2, 1, Tin, Tout>(L, s);
+        case 4: return launch_flush_w<4, 1, Tin, Tout>(L, s);
+        case 8: return launch_flush_w<8, 1, Tin, Tout>(L, s);
+        case 16: return launch_flush_w<16, 1, Tin, Tout>(L, s);
+        default: return launch_flush_w<0, 1, Tin, Tout>(L, s);
+    }
+}
+
+}  // namespace dpred
