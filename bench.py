@@ -151,14 +151,20 @@ def barrier(ws):
         dist.barrier()
 
 
-def max_over_ranks(x: float, ws: int) -> float:
+def max_over_ranks(x: float, ws: int, device: str = "cuda") -> float:
+    """The slowest rank's time: every rank's clock ran over the same barrier-bracketed region."""
     if ws == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_gbs(ws: int, step_bytes: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job GB/s: the bytes every rank processed over the slowest rank's time."""
+    return ws * step_bytes * steps / (elapsed_ms * 1e-3) / 1e9
 
 
 # ----------------------------------------------------------- the workload ---
@@ -205,7 +211,7 @@ def run_dpred(args):
 
     ws, rank, local = dist_setup(args.gpus)
     tree, layout, buckets = flush_workload(args.max_buckets)
-    n_rows = tree.total
+    n_rows = max(b.start + b.size for b in buckets)  # the whole row unless --max-buckets trims it
     stream = torch.cuda.current_stream()
     grads = torch.empty((WORLD, n_rows), dtype=torch.bfloat16, device="cuda")
     datagen.fill_device(grads.data_ptr(), WORLD, n_rows, n_rows, BF16, NORMAL, SEED, 0, 1, 0, SIGMA,
@@ -248,7 +254,7 @@ def run_dpred(args):
     launch_ms = sum(per_launch[j].elapsed_time(per_launch[j + 1]) for j in range(0, len(per_launch), 2))
     avg_launch_ms = launch_ms / (launches_per_step * args.steps)
     elapsed_max = max_over_ranks(elapsed_ms, ws)
-    value_gbs = ws * step_bytes * args.steps / (elapsed_max * 1e-3) / 1e9
+    value_gbs = job_gbs(ws, step_bytes, args.steps, elapsed_max)
     elems_per_s = ws * step_elems * args.steps / (elapsed_max * 1e-3)
 
     peak, peak_src = peaks()
@@ -268,7 +274,7 @@ def run_dpred(args):
         "algorithmic_bytes_per_step": step_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "flush_kernel<8,2,bf16,bf16,FlushArgsInline>", "bytes_per_launch": bytes_per_launch,
+                     "kernel": "flush_kernel<8,1,bf16,bf16,FlushArgsInline>", "bytes_per_launch": bytes_per_launch,
                      "avg_launch_ms": round(avg_launch_ms, 5)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -340,11 +346,11 @@ def _cpu_flush_sample(buckets, tree, seconds):
             p = int(task["param_id"])
             for r in range(om["holder_lo"][p], om["holder_hi"][p] + 1):
                 dst[r][t] = np.empty(int(task["numel"]), np.uint16)
-            writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else om["holder_hi"][p] - om["holder_lo"][p] + 1)
+            writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else int(om["holder_hi"][p] - om["holder_lo"][p]) + 1)
         t0 = time.perf_counter()
         oracle.flush(WORLD, host, b.tasks, om["owner"], tree.n_params, dst, BF16, True, True)
         done_s += time.perf_counter() - t0
-        done_bytes += WORLD * b.size * 2 + writes * 2
+        done_bytes += WORLD * int(b.size) * 2 + int(writes) * 2
         done_elems += b.size
         n_b += 1
         if done_s >= seconds:
@@ -541,7 +547,7 @@ def _oracle_step(host, tasks, om, tree):
         p = int(task["param_id"])
         for r in range(om["holder_lo"][p], om["holder_hi"][p] + 1):
             dst[r][t] = np.empty(int(task["numel"]), np.uint16)
-        writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else om["holder_hi"][p] - om["holder_lo"][p] + 1)
+        writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else int(om["holder_hi"][p] - om["holder_lo"][p]) + 1)
     oracle.flush(WORLD, host, tasks, om["owner"], tree.n_params, dst, BF16, True, True)
     return WORLD * host.shape[1] * 2 + writes * 2
 
