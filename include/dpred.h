@@ -178,6 +178,34 @@ int dpred_flush_bucket(int32_t world, int32_t in_dtype, void* grads, int64_t ld,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Allocation-free bucket flush.  The pages have no counterpart to this entry
+ * point; it serves callers that cannot allocate device memory: code that
+ * runs while a CUDA graph is being captured, runtimes that carve all device
+ * memory out of a fixed budget up front, and plug-ins that live inside
+ * another framework's allocator.
+ *
+ * Same arguments and results as dpred_flush_bucket, minus the workspace.  A
+ * bucket whose task table does not fit inside the launch uses a scratch
+ * array of DPRED_NOALLOC_SCRATCH_BYTES (1 MiB) compiled into the library;
+ * every GPU that loads the library holds that array until the process exits.
+ * Buckets with dpred_flush_workspace_bytes(world, n_tasks) above
+ * DPRED_NOALLOC_SCRATCH_BYTES are rejected with DPRED_E_SIZE before anything
+ * is enqueued.  The call allocates no device memory.
+ * Set-up: the first call made on a device looks up the scratch array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.
+ * Sharing: all calls use the same scratch array, and each call overwrites the
+ * part it uses (nothing in it has to start at zero).  Calls whose work can
+ * overlap on the GPU -- on different streams without ordering between them --
+ * race on the array; issue them on one stream or order them with events.
+ */
+#define DPRED_NOALLOC_SCRATCH_BYTES (1u << 20)
+int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int64_t ld, const dpred_task* tasks,
+                               int32_t n_tasks, const int32_t* owner, int32_t n_params, int32_t out_dtype,
+                               void* const* dst, int32_t pre_div, int32_t reduce_to_owner, int32_t checked,
+                               dpred_probe* probe, void* stream);
+
+/*
  * Replica-local gradient accumulation with one cross-replica reduction per
  * optimizer step.  [MT] "What" (cotangents come out unreduced, a per-replica
  * partial sum that accumulates replica-locally across micro-batches; update()

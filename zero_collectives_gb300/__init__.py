@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
         L.dpred_flush_workspace_bytes.argtypes = [i32, i32]
         L.dpred_flush_bucket.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp, vp,
                                          ctypes.c_size_t, vp]
+        L.dpred_flush_bucket_noalloc.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp,
+                                                 vp]
         L.dpred_accumulate_microbatch.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp, vp]
         L.dpred_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32, vp]
         L.dpred_allgather.argtypes = [i32, i64, i32, vp, vp, i32, vp]
@@ -247,6 +249,32 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
                                     out_dt, None if dst is None else dst.c, int(pre_div), int(reduce_to_owner),
                                     int(checked), None if p is None else ctypes.byref(p), ws_ptr, ws_bytes,
                                     _stream(stream)))
+    return _probe_from(p, world) if p is not None else None
+
+
+def flush_bucket_noalloc(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
+                         pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False,
+                         probe: bool = False, flush_index: int = 0, stream=None):
+    """flush_bucket for callers that cannot allocate device memory (e.g. under
+    CUDA graph capture or inside a fixed device budget): no workspace, the
+    library's own 1 MiB scratch holds large task tables.  Calls that overlap on
+    the GPU share that scratch, so issue them on one stream."""
+    if grads.dim() != 2 or grads.stride(1) != 1:
+        raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
+    world = grads.shape[0]
+    in_dt = _dtype_code(grads)
+    out_dt = in_dt if out_dtype is None else out_dtype
+    ld = grads.stride(0) if world > 1 else grads.shape[1]
+    t = _tasks_arg(tasks)
+    own = None if owner is None else np.ascontiguousarray(owner, dtype=np.int32)
+    p = _Probe() if probe else None
+    if p is not None:
+        p.flush_index = flush_index
+    _check(lib().dpred_flush_bucket_noalloc(world, in_dt, grads.data_ptr(), ld, t.ctypes.data, len(t),
+                                            None if own is None else own.ctypes.data,
+                                            0 if own is None else len(own), out_dt,
+                                            None if dst is None else dst.c, int(pre_div), int(reduce_to_owner),
+                                            int(checked), None if p is None else ctypes.byref(p), _stream(stream)))
     return _probe_from(p, world) if p is not None else None
 
 
