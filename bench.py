@@ -47,6 +47,13 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--flush-path", choices=["auto", "ldg", "tma"], default="auto",
+                    help="kernel family of the flush (results are bit-identical)")
+    ap.add_argument("--row", choices=["allgather", "reduce_scatter", "accumulate"], default=None,
+                    help="time one other hot-path row alone (small profiling cases) and print its JSON line")
+    ap.add_argument("--row-nodes", type=int, default=8)
+    ap.add_argument("--row-elems", type=int, default=1 << 29,
+                    help="--row size: M (allgather / reduce_scatter) or n (accumulate, W=4)")
     return ap.parse_args()
 
 
@@ -131,6 +138,16 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def smi_gpu_id(logical: int) -> str:
+    """nvidia-smi's id of a CUDA device (physical index or UUID under CUDA_VISIBLE_DEVICES)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if logical < len(ids):
+            return ids[logical]
+    return str(logical)
+
+
 def dist_setup(gpus: int):
     import torch
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -210,6 +227,7 @@ def run_dpred(args):
     from datagen import BF16, NORMAL
 
     ws, rank, local = dist_setup(args.gpus)
+    zc.set_flush_path({"auto": zc.PATH_AUTO, "ldg": zc.PATH_LDG, "tma": zc.PATH_TMA}[args.flush_path])
     tree, layout, buckets = flush_workload(args.max_buckets)
     n_rows = max(b.start + b.size for b in buckets)  # the whole row unless --max-buckets trims it
     stream = torch.cuda.current_stream()
@@ -230,29 +248,22 @@ def run_dpred(args):
         step()
     torch.cuda.synchronize()
 
-    clocks = Clocks(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks = Clocks(smi_gpu_id(torch.cuda.current_device()))
     clocks.start()
     barrier(ws)
     torch.cuda.synchronize()
     ev_start, ev_end = events(2)
-    per_launch = events(2 * launches_per_step * args.steps)
     ev_start.record(stream)
-    i = 0
     for _ in range(args.steps):
-        zc.build_owner_map(WORLD, [(None, tree.numel)], True)
-        for (start, tasks), size, table in zip(ex.buckets, ex.sizes, ex.tables):
-            per_launch[i].record(stream)
-            zc.flush_bucket(grads[:, start:start + size], tasks, ex.omap.owner, table, zc.BF16, True, True,
-                            probe=True, workspace=ex.workspace, stream=stream)
-            per_launch[i + 1].record(stream)
-            i += 2
+        step()
     ev_end.record(stream)
     torch.cuda.synchronize()
     barrier(ws)
     clk = clocks.stop()
     elapsed_ms = ev_start.elapsed_time(ev_end)
-    launch_ms = sum(per_launch[j].elapsed_time(per_launch[j + 1]) for j in range(0, len(per_launch), 2))
-    avg_launch_ms = launch_ms / (launches_per_step * args.steps)
+    # The timed region launches nothing but the flush kernel, so its mean
+    # launch duration is the region time over the launches (gaps included).
+    avg_launch_ms = elapsed_ms / (launches_per_step * args.steps)
     elapsed_max = max_over_ranks(elapsed_ms, ws)
     value_gbs = job_gbs(ws, step_bytes, args.steps, elapsed_max)
     elems_per_s = ws * step_elems * args.steps / (elapsed_max * 1e-3)
@@ -288,6 +299,7 @@ def run_dpred(args):
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(buckets, tree, layout, args.cpu_seconds)
     if not args.no_rows:
+        result["flush_paths"] = flush_path_ab(ex, grads, step_bytes, peak)
         del grads
         result["rows"] = rows(peak)
     if rank == 0:
@@ -365,6 +377,20 @@ def cpu_baseline(buckets, tree, layout, seconds):
     return {"value": round(nbytes / secs / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{nb} of {len(buckets)} buckets ({elems} elements per replica row), single-threaded C oracle",
             "seconds": round(secs, 2), "grad_elems_per_s": round(elems / secs, 1)}
+
+
+def flush_path_ab(ex, grads, step_bytes, peak):
+    """The same flush step with each kernel family (LDG streaming vs TMA staging)."""
+    import zero_collectives_gb300 as zc
+    out = {}
+    prev = zc.set_flush_path(zc.PATH_LDG)
+    for name, path in (("ldg", zc.PATH_LDG), ("tma", zc.PATH_TMA)):
+        zc.set_flush_path(path)
+        ms = timed(lambda: ex.flush_all(grads), 20, warm=3)
+        gbs = step_bytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms_per_step": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
+    zc.set_flush_path(prev)
+    return out
 
 
 # -------------------------------------------------------- other hot rows ---
@@ -466,11 +492,24 @@ def rows(peak):
         rs = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
         ms = timed(lambda: zc.reduce_scatter(x, rs), 10)
         out[f"reduce_scatter_N{N}"] = entry(ms, N * Mel * 2 + Mel * 2, workload=f"N={N}, M=1 GiB bf16")
+        prev = zc.set_flush_path(zc.PATH_TMA)
+        ms = timed(lambda: zc.reduce_scatter(x, rs), 10)
+        zc.set_flush_path(prev)
+        out[f"reduce_scatter_N{N}_tma"] = entry(ms, N * Mel * 2 + Mel * 2, workload=f"N={N}, M=1 GiB bf16, TMA path")
         del x
         ag = torch.empty((N, Mel), dtype=torch.bfloat16, device="cuda")
         for order, name in ((0, "canonical"), (1, "ring")):
             ms = timed(lambda: zc.allgather(rs, ag, order), 10)
-            out[f"allgather_{name}_N{N}"] = entry(ms, Mel * 2 + N * Mel * 2, workload=f"N={N}, M=1 GiB bf16")
+            out[f"allgather_{name}_N{N}"] = entry(ms, Mel * 2 + N * Mel * 2, workload=f"N={N}, M=1 GiB bf16 (TMA form)")
+            prev = zc.set_flush_path(zc.PATH_LDG)
+            ms = timed(lambda: zc.allgather(rs, ag, order), 10)
+            zc.set_flush_path(prev)
+            out[f"allgather_{name}_N{N}_ldg"] = entry(ms, Mel * 2 + N * Mel * 2,
+                                                      workload=f"N={N}, M=1 GiB bf16, register-streaming form")
+        wr = torch.empty(N * Mel, dtype=torch.bfloat16, device="cuda")
+        ms = timed(lambda: wr.zero_(), 10)
+        out[f"torch_zero_fill_{N}GiB"] = entry(ms, N * Mel * 2, workload="write-only reference (torch zero_)")
+        del wr
         del ag, rs
     torch.cuda.empty_cache()
     return out
@@ -552,9 +591,50 @@ def _oracle_step(host, tasks, om, tree):
     return WORLD * host.shape[1] * 2 + writes * 2
 
 
+def single_row(args):
+    """One row alone, e.g. for an ncu capture of a small case."""
+    import torch
+    import datagen
+    import zero_collectives_gb300 as zc
+    from datagen import F32, NORMAL, UNIFORM, BF16, stream_id
+    torch.cuda.set_device(0)
+    zc.set_flush_path({"auto": zc.PATH_AUTO, "ldg": zc.PATH_LDG, "tma": zc.PATH_TMA}[args.flush_path])
+    s = torch.cuda.current_stream().cuda_stream
+    peak, _ = peaks()
+    N, M = args.row_nodes, args.row_elems
+    if args.row in ("allgather", "reduce_scatter"):
+        S = M // N
+        if args.row == "allgather":
+            x = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
+            datagen.fill_device(x.data_ptr(), N, S, S, BF16, UNIFORM, 5, 0, 1, 0, 1.0, s)
+            out = torch.empty((N, N * S), dtype=torch.bfloat16, device="cuda")
+            fn = lambda: zc.allgather(x, out, 0)  # noqa: E731
+            nbytes = N * S * 2 + N * N * S * 2
+        else:
+            x = torch.empty((N, N * S), dtype=torch.bfloat16, device="cuda")
+            datagen.fill_device(x.data_ptr(), N, N * S, N * S, BF16, UNIFORM, 5, 0, 1, 0, 1.0, s)
+            out = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
+            fn = lambda: zc.reduce_scatter(x, out)  # noqa: E731
+            nbytes = N * N * S * 2 + N * S * 2
+    else:
+        W, n = 4, M
+        acc = torch.empty((W, n), dtype=torch.float32, device="cuda")
+        g = torch.empty((W, n), dtype=torch.float32, device="cuda")
+        datagen.fill_device(g.data_ptr(), W, n, n, F32, NORMAL, 4, stream_id(0, 0), 1, 0, SIGMA, s)
+        acc.zero_()
+        fn = lambda: zc.accumulate_microbatch(acc, g, first=False, finalize=False)  # noqa: E731
+        nbytes = 12 * W * n
+    ms = timed(fn, max(args.steps, 1), warm=max(args.warmup, 3))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"row": args.row, "nodes": N, "elems": M, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                      "frac_of_peak": round(gbs / peak, 4), "bytes": nbytes}), flush=True)
+
+
 def main():
     args = parse()
-    if args.impl == "reference":
+    if args.row is not None:
+        single_row(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_dpred(args)

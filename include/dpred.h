@@ -254,11 +254,39 @@ int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const v
                     void* stream);
 
 /*
+ * Kernel family used by later dpred_flush_bucket, dpred_reduce_scatter and
+ * dpred_allgather calls in this process (a tuning knob; results are
+ * bit-identical either way):
+ *   0 auto (the default: the family measured fastest on GB300 for each call:
+ *     register streaming for the flush and ReduceScatter, TMA for AllGather),
+ *   1 register streaming: every thread keeps one 16-byte load per replica row
+ *     (flush) or per shard (AllGather) in flight and stores from registers,
+ *   2 TMA staging: the flush has one thread per SM stream 4 KB row tiles into a
+ *     ring of shared-memory stages with cp.async.bulk (mbarrier-counted) while
+ *     eight warps reduce from shared memory (world in {2, 4, 8, 16} only;
+ *     other world sizes use family 1); AllGather bulk-loads 16 KB shard tiles
+ *     into shared memory once and bulk-stores each to its N destinations
+ *     (16-byte aligned shards only).
+ * Returns the previous setting, or DPRED_E_INVAL.  Not thread-safe against
+ * concurrent flush calls.
+ */
+int dpred_set_flush_path(int32_t path);
+
+/*
  * Device error word: 0, or the DPRED_E_* code of the first device-side
  * failure (a bounded wait that gave up, an internal consistency check) since
  * the last clear.  Synchronises the current device.  clear != 0 resets it.
  */
 int dpred_device_status(int32_t* code, int32_t clear);
+
+/*
+ * Self-test of the bounded-wait path (no counterpart in the pages): launches
+ * one thread that waits on an mbarrier phase nothing completes, gives up after
+ * budget_cycles SM clocks (0..4e9) and records DPRED_E_TIMEOUT in the device
+ * error word, read back with dpred_device_status.  No fault, no trap: the
+ * context stays usable.  Asynchronous on `stream`.
+ */
+int dpred_selftest_wait_timeout(int64_t budget_cycles, void* stream);
 
 #ifdef __cplusplus
 }

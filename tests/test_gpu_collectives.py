@@ -14,6 +14,14 @@ from tests.gpu_util import TORCH_DT, device_matrix, np_bits, to_bits
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(params=[zc.PATH_LDG, zc.PATH_TMA], ids=["ldg", "tma"], autouse=True)
+def flush_path(request):
+    """Run every test with both flush kernel families (results must be bit-identical)."""
+    prev = zc.set_flush_path(request.param)
+    yield request.param
+    zc.set_flush_path(prev)
+
+
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("in_dt,out_dt", [(BF16, BF16), (F32, F32), (BF16, F32)])
 @pytest.mark.parametrize("pre_div", [False, True])

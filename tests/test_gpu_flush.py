@@ -18,6 +18,14 @@ from tests.helpers import holder_sets, is_sentinel
 
 pytestmark = pytest.mark.gpu
 
+
+@pytest.fixture(params=[zc.PATH_LDG, zc.PATH_TMA], ids=["ldg", "tma"], autouse=True)
+def flush_path(request):
+    """Run every test with both flush kernel families (results must be bit-identical)."""
+    prev = zc.set_flush_path(request.param)
+    yield request.param
+    zc.set_flush_path(prev)
+
 GUARD = 16  # canary elements before and after every destination
 
 

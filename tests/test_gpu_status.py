@@ -1,0 +1,26 @@
+"""The device error word and the bounded-wait path, exercised without any
+fault: a kernel waits on a barrier that nothing completes and must give up
+after its budget with DPRED_E_TIMEOUT, leaving the context usable."""
+import pytest
+import torch
+
+import zero_collectives_gb300 as zc
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    assert zc.device_status(clear=True) in (0, -6)
+    assert zc.device_status() == 0
+    zc.selftest_wait_timeout(2_000_000)   # about 1 ms of SM clocks
+    torch.cuda.synchronize()
+    assert zc.device_status() == -6
+    assert zc.device_status(clear=True) == -6
+    assert zc.device_status() == 0
+    x = torch.ones(1024, device="cuda")
+    assert float(x.sum().item()) == 1024.0   # the context still works
+
+
+def test_selftest_rejects_bad_budget():
+    with pytest.raises(zc.DpredError):
+        zc.selftest_wait_timeout(-1)

@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.dpred_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32, vp]
         L.dpred_allgather.argtypes = [i32, i64, i32, vp, vp, i32, vp]
         L.dpred_device_status.argtypes = [vp, i32]
+        L.dpred_set_flush_path.argtypes = [i32]
+        L.dpred_selftest_wait_timeout.argtypes = [i64, vp]
         _lib = L
     return _lib
 
@@ -314,6 +316,22 @@ def allgather(inp, out, order: int = 0, stream=None):
     _check(lib().dpred_allgather(N, S, _dtype_code(inp), inp.data_ptr(), out.data_ptr(), int(order),
                                  _stream(stream)))
     return out
+
+
+PATH_AUTO, PATH_LDG, PATH_TMA = 0, 1, 2
+
+
+def set_flush_path(path: int) -> int:
+    """Kernel family of later flushes: PATH_AUTO, PATH_LDG or PATH_TMA.  Returns the previous one."""
+    rc = lib().dpred_set_flush_path(int(path))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def selftest_wait_timeout(budget_cycles: int = 2_000_000, stream=None) -> None:
+    """Launch a kernel whose bounded wait must give up (see dpred_selftest_wait_timeout)."""
+    _check(lib().dpred_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
 
 
 def device_status(clear: bool = False) -> int:

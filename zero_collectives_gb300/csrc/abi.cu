@@ -16,6 +16,12 @@ namespace dpred {
 __device__ int g_device_error;  // first device-side failure code, 0 when none
 
 namespace {
+int g_flush_path = PATH_AUTO;
+}
+
+int flush_path() { return g_flush_path; }
+
+namespace {
 thread_local std::string t_last_error;
 
 int elem_size(int dt) { return dt == DPRED_BF16 ? 2 : 4; }
@@ -62,6 +68,7 @@ int run_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, in
     if (plan.empty()) return DPRED_OK;
     FlushLaunch L{};
     L.h.grads = grads;
+    L.h.err = device_error_word();
     L.h.ld = ld;
     L.h.total_units = units;
     L.h.world = world;
@@ -108,9 +115,15 @@ int sm_count() {
 }
 
 int* device_error_word() {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    return static_cast<int*>(p);
+    static int* cached[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cached[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<int*>(p);
+    }
+    return cached[dev];
 }
 
 }  // namespace dpred
@@ -335,6 +348,14 @@ int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const v
     if ((in && !aligned(in, esz)) || (out && !aligned(out, esz)))
         return set_error(DPRED_E_ALIGN, "pointer not aligned to its element size");
     return launch_allgather(n_nodes, shard_elems, esz, in, out, order, static_cast<cudaStream_t>(stream));
+}
+
+int dpred_set_flush_path(int32_t path) {
+    if (path != PATH_AUTO && path != PATH_LDG && path != PATH_TMA)
+        return set_error(DPRED_E_INVAL, "flush path %d: 0 (auto), 1 (LDG) or 2 (TMA)", path);
+    int prev = g_flush_path;
+    g_flush_path = path;
+    return prev;
 }
 
 int dpred_device_status(int32_t* code, int32_t clear) {

@@ -69,6 +69,7 @@ static_assert(sizeof(TaskDesc) == 32, "TaskDesc layout");
 
 struct FlushHeader {
     const void* grads;
+    int* err;            // device error word (bounded waits that give up record DPRED_E_TIMEOUT)
     int64_t ld;          // row stride in elements
     int64_t total_units;
     int32_t world;
@@ -96,7 +97,7 @@ struct FlushArgsWs {
 };
 
 constexpr int kFlushThreads = 256;
-constexpr int kUnitVec = 1024;     // 16-byte vectors per work unit of the vector path
+constexpr int kUnitVec = 256;      // 16-byte vectors per work unit of the vector path (4 KB per row)
 constexpr int kUnitScalar = 2048;  // elements per work unit of the scalar path
 
 struct FlushLaunch {
@@ -129,5 +130,9 @@ int launch_allgather(int n_nodes, int64_t shard_elems, int esize, const void* in
                      cudaStream_t s);
 
 int* device_error_word();  // device address of the error word (current device)
+
+// Kernel family used by the bucket flush (and ReduceScatter): see dpred_set_flush_path.
+enum FlushPath : int { PATH_AUTO = 0, PATH_LDG = 1, PATH_TMA = 2 };
+int flush_path();
 
 }  // namespace dpred

@@ -10,7 +10,7 @@
 // rows whose store goes straight into the delivered, non-empty destinations:
 // the copy-out is fused into the store.
 //
-// Work decomposition: the host cuts every task into work units (1024 16-byte
+// Work decomposition: the host cuts every task into work units (256 16-byte
 // vectors on the vector path, 2048 elements on the scalar path); a persistent
 // grid strides over units in bucket order and finds each unit's task by a
 // binary search over the plan (all threads of a CTA read the same entries, a
@@ -19,6 +19,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "tma.cuh"
 
 namespace dpred {
 
@@ -185,19 +186,25 @@ __device__ __forceinline__ void flush_unit(const Args& a, const TaskDesc& T, int
     }
 }
 
+// The plan task that work unit u belongs to: the last task whose first unit is <= u.
+template <typename Args>
+__device__ __forceinline__ int find_task(const Args& a, int64_t u) {
+    int lo = 0, hi = a.h.n_tasks - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (plan_task(a, mid).unit_begin <= u)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
 __global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_constant__ Args a) {
     const FlushHeader& h = a.h;
     for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
-        int lo = 0, hi = h.n_tasks - 1;  // last task with unit_begin <= u
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (plan_task(a, mid).unit_begin <= u)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const TaskDesc T = plan_task(a, lo);
+        const TaskDesc T = plan_task(a, find_task(a, u));
         const int64_t local = u - T.unit_begin;
         if (h.pdiv == PDIV_POW2)
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_POW2>(a, T, local);
@@ -206,6 +213,171 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_const
         else
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE>(a, T, local);
     }
+}
+
+// ---------------------------------------------------------------------------
+// TMA-staged flush.  One producer thread per CTA streams the W row tiles of
+// every sub-tile (kSubVec 16-byte vectors = 4 KB per row) into a ring of
+// shared-memory stages with cp.async.bulk, each stage's arrival counted on its
+// `full` mbarrier; eight consumer warps reduce a stage from shared memory (one
+// vector per thread, rank order), store the result to the delivered
+// destinations and release the stage on its `empty` mbarrier.  The ring keeps
+// up to 192 KB of every SM's share of the bucket in flight without holding it
+// in registers.  Scalar work (heads, tails, tasks that are not co-aligned) is
+// done by the consumers straight from global memory, as in flush_kernel.
+// ---------------------------------------------------------------------------
+
+constexpr int kTmaConsumerWarps = 8;
+constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
+constexpr int kTmaThreads = kTmaConsumers + 32;
+constexpr int kSubVec = 256;                  // 16-byte vectors per row per stage
+constexpr uint32_t kTmaRowBytes = kSubVec * 16;
+constexpr int kTmaStageBudget = 192 * 1024;   // shared memory given to the stage ring
+
+template <int W>
+__host__ __device__ constexpr int tma_stages() {
+    constexpr int s = kTmaStageBudget / (W * (int)kTmaRowBytes);
+    return s > 16 ? 16 : (s < 2 ? 2 : s);
+}
+
+template <int W>
+__host__ __device__ constexpr size_t tma_smem_bytes() {
+    return (size_t)tma_stages<W>() * W * kTmaRowBytes;
+}
+
+__device__ __forceinline__ void record_device_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+template <int W_T, typename Tin, typename Tout, int MODE, typename Args>
+__device__ void tma_consume(const Args& a, unsigned char* smem, uint64_t* full, uint64_t* empty, int* abort_flag) {
+    constexpr int VEC = Elem<Tin>::kVec;
+    constexpr int STAGES = tma_stages<W_T>();
+    const FlushHeader& h = a.h;
+    const int ctid = threadIdx.x, lane = threadIdx.x & 31;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
+        const TaskDesc T = plan_task(a, find_task(a, u));
+        const int64_t local = u - T.unit_begin;
+        if (!T.vec) {
+            const int64_t e0 = local * kUnitScalar;
+            const int64_t e1 = e0 + kUnitScalar < T.numel ? e0 + kUnitScalar : T.numel;
+            for (int64_t k = e0 + ctid; k < e1; k += kTmaConsumers) flush_element<Tin, Tout, MODE>(a, T, k);
+            continue;
+        }
+        const int64_t nbody = (T.numel - T.head) / VEC;
+        const int64_t v0 = local * kUnitVec;
+        const int64_t v1 = v0 + kUnitVec < nbody ? v0 + kUnitVec : nbody;
+        if (local == 0) {
+            const int tail = (int)(T.numel - T.head - nbody * VEC);
+            if (ctid < T.head)
+                flush_element<Tin, Tout, MODE>(a, T, ctid);
+            else if (ctid < T.head + tail)
+                flush_element<Tin, Tout, MODE>(a, T, T.head + nbody * VEC + (ctid - T.head));
+        }
+        for (int64_t sv = v0; sv < v1; sv += kSubVec) {
+            const int64_t nv = v1 - sv < kSubVec ? v1 - sv : kSubVec;
+            if (!tma::mbar_wait(&full[stage], phase)) {
+                *reinterpret_cast<volatile int*>(abort_flag) = 1;
+                record_device_error(h.err, DPRED_E_TIMEOUT);
+                return;
+            }
+            if (ctid < nv) {
+                const unsigned char* tile = smem + (size_t)stage * W_T * kTmaRowBytes + (size_t)ctid * 16;
+                float y[VEC];
+#pragma unroll
+                for (int r = 0; r < W_T; ++r) {
+                    const uint4 q = *reinterpret_cast<const uint4*>(tile + (size_t)r * kTmaRowBytes);
+                    fold<Tin, MODE>(y, q, r == 0, h.wf, h.inv_w);
+                }
+                const int64_t e = T.head + (sv + ctid) * VEC;
+                for (int d = 0; d < T.ndst; ++d)
+                    store_vec<Tout, VEC>(static_cast<Tout*>(plan_dst(a, T.dst_begin + d)) + e, y);
+            }
+            __syncwarp();
+            if (lane == 0) tma::mbar_arrive(&empty[stage]);
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+    }
+}
+
+template <int W_T, typename Tin, typename Tout, typename Args>
+__device__ void tma_produce(const Args& a, unsigned char* smem, uint64_t* full, uint64_t* empty, int* abort_flag) {
+    constexpr int VEC = Elem<Tin>::kVec;
+    constexpr int STAGES = tma_stages<W_T>();
+    const FlushHeader& h = a.h;
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < h.total_units; u += gridDim.x) {
+        const TaskDesc T = plan_task(a, find_task(a, u));
+        if (!T.vec) continue;
+        const int64_t local = u - T.unit_begin;
+        const int64_t nbody = (T.numel - T.head) / VEC;
+        const int64_t v0 = local * kUnitVec;
+        const int64_t v1 = v0 + kUnitVec < nbody ? v0 + kUnitVec : nbody;
+        const char* base = reinterpret_cast<const char*>(static_cast<const Tin*>(h.grads) + T.src_off + T.head);
+        const int64_t row_bytes = h.ld * (int64_t)sizeof(Tin);
+        for (int64_t sv = v0; sv < v1; sv += kSubVec) {
+            const uint32_t bytes = (uint32_t)((v1 - sv < kSubVec ? v1 - sv : kSubVec) * 16);
+            if (*reinterpret_cast<volatile int*>(abort_flag) || !tma::mbar_wait(&empty[stage], phase ^ 1)) {
+                ok = false;
+                break;
+            }
+            tma::mbar_arrive_expect_tx(&full[stage], bytes * W_T);
+#pragma unroll
+            for (int r = 0; r < W_T; ++r)
+                tma::bulk_load(smem + ((size_t)stage * W_T + r) * kTmaRowBytes, base + r * row_bytes + sv * 16, bytes,
+                               &full[stage]);
+            ++issued;
+            if (++stage == STAGES) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
+    }
+    if (!ok) record_device_error(h.err, DPRED_E_TIMEOUT);
+    // Leave only after every bulk copy this thread issued has landed.
+    const int64_t pend = issued < STAGES ? issued : STAGES;
+    for (int64_t q = issued - pend; q < issued; ++q)
+        if (!tma::mbar_wait(&full[q % STAGES], (uint32_t)((q / STAGES) & 1))) {
+            record_device_error(h.err, DPRED_E_TIMEOUT);
+            break;
+        }
+}
+
+template <int W_T, typename Tin, typename Tout, typename Args>
+__global__ void __launch_bounds__(kTmaThreads, 1) flush_tma_kernel(const __grid_constant__ Args a) {
+    constexpr int STAGES = tma_stages<W_T>();
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[STAGES];
+    __shared__ __align__(8) uint64_t empty[STAGES];
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            tma::mbar_init(&full[s], 1);
+            tma::mbar_init(&empty[s], kTmaConsumerWarps);
+        }
+        abort_flag = 0;
+        tma::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x >= kTmaConsumers) {
+        if (threadIdx.x == kTmaConsumers) tma_produce<W_T, Tin, Tout>(a, smem, full, empty, &abort_flag);
+        return;
+    }
+    const int mode = a.h.pdiv;
+    if (mode == PDIV_POW2)
+        tma_consume<W_T, Tin, Tout, PDIV_POW2>(a, smem, full, empty, &abort_flag);
+    else if (mode == PDIV_DIV)
+        tma_consume<W_T, Tin, Tout, PDIV_DIV>(a, smem, full, empty, &abort_flag);
+    else
+        tma_consume<W_T, Tin, Tout, PDIV_NONE>(a, smem, full, empty, &abort_flag);
 }
 
 // Persistent grid: SMs x resident CTAs (queried once per kernel), capped by the number of units.
@@ -221,17 +393,41 @@ int64_t persistent_grid(K kernel, int64_t units) {
     return units < g ? units : g;
 }
 
+// One launch of the LDG kernel (any W) or, for W in {2, 4, 8, 16} when the
+// TMA path is selected, of the TMA-staged kernel (one CTA per SM).
+template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
+cudaError_t launch_kernel(const Args& a, int64_t units, cudaStream_t s) {
+    if constexpr (W_T > 0) {
+        if (flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
+            auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
+            constexpr size_t smem = tma_smem_bytes<W_T>();
+            static bool attr = false;
+            if (!attr) {
+                cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+                attr = true;
+            }
+            int64_t g = sm_count();
+            k<<<(unsigned)(units < g ? units : g), kTmaThreads, smem, s>>>(a);
+            return cudaGetLastError();
+        }
+    }
+    auto k = flush_kernel<W_T, BATCH, Tin, Tout, Args>;
+    k<<<(unsigned)persistent_grid(k, units), kFlushThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
 template <int W_T, int BATCH, typename Tin, typename Tout>
 int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
     const FlushHeader& h = L.h;
     if (h.total_units == 0) return DPRED_OK;
+    cudaError_t e;
     if (h.n_tasks <= kInlineTasks && L.n_dst <= kInlineDst) {
         FlushArgsInline a;
         a.h = h;
         for (int i = 0; i < h.n_tasks; ++i) a.tasks[i] = L.tasks[i];
         for (int i = 0; i < L.n_dst; ++i) a.dst[i] = L.dst[i];
-        auto k = flush_kernel<W_T, BATCH, Tin, Tout, FlushArgsInline>;
-        k<<<(unsigned)persistent_grid(k, h.total_units), kFlushThreads, 0, s>>>(a);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, s);
     } else {
         size_t tb = sizeof(TaskDesc) * (size_t)h.n_tasks, db = sizeof(void*) * (size_t)L.n_dst;
         size_t need = tb + ((db + 15) & ~(size_t)15);
@@ -241,17 +437,15 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         if ((reinterpret_cast<uintptr_t>(L.workspace) & 15) != 0)
             return set_error(DPRED_E_ALIGN, "flush workspace must be 16-byte aligned");
         char* ws = static_cast<char*>(L.workspace);
-        cudaError_t e = cudaMemcpyAsync(ws, L.tasks, tb, cudaMemcpyHostToDevice, s);
+        e = cudaMemcpyAsync(ws, L.tasks, tb, cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess && db) e = cudaMemcpyAsync(ws + tb, L.dst, db, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_error(e, "flush plan copy");
         FlushArgsWs a;
         a.h = h;
         a.tasks = reinterpret_cast<const TaskDesc*>(ws);
         a.dst = reinterpret_cast<void* const*>(ws + tb);
-        auto k = flush_kernel<W_T, BATCH, Tin, Tout, FlushArgsWs>;
-        k<<<(unsigned)persistent_grid(k, h.total_units), kFlushThreads, 0, s>>>(a);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, s);
     }
-    cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
 }
 
