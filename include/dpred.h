@@ -227,6 +227,22 @@ int dpred_accumulate_microbatch(int32_t world, int64_t n, float* acc, int32_t g_
                                 int32_t first, int32_t finalize, float scale, float* total, void* stream);
 
 /*
+ * Accumulator checkpoints.  [MT] "What else had to change", "Accumulator
+ * lifetime": a checkpoint holds the reduced total, so saving runs the pending
+ * cross-replica all-reduce; restoring moves a total back onto the unreduced
+ * form by leaving it on one replica and zeros on the rest, so that the next
+ * deferred reduction reproduces it.
+ *   dpred_accumulator_save:    total[k] = acc[0][k] + ... + acc[W-1][k]
+ *                              (rank order, fp32, no scale); acc is not changed.
+ *   dpred_accumulator_restore: acc[0][k] = total[k]; acc[r][k] = +0 for r > 0.
+ * acc (device) is [world, n] fp32 row-contiguous, total (device) is [n] fp32.
+ * Restore followed by save returns the total bit for bit (a -0 becomes +0).
+ * Errors: DPRED_E_INVAL, DPRED_E_ALIGN, DPRED_E_CUDA.  Asynchronous on `stream`.
+ */
+int dpred_accumulator_save(int32_t world, int64_t n, const float* acc, float* total, void* stream);
+int dpred_accumulator_restore(int32_t world, int64_t n, float* acc, const float* total, void* stream);
+
+/*
  * ReduceScatter.  [AG] "与 ReduceScatter 的对偶关系" (duality table: M
  * elements in per node, M/N out per node, reduce then shard).
  * in (device) is [n_nodes, m_elems] of in_dtype; out (device) is

@@ -41,6 +41,8 @@ def lib():
         L.orc_flush.argtypes = [i32, i32, vp, i64, i32, vp, vp, vp, vp, i32, i32, vp, i32, i32, vp]
         L.orc_flush_probe.argtypes = [i32, i32, vp, vp, vp, i32, vp, i32, vp]
         L.orc_accumulate.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp]
+        L.orc_accumulator_save.argtypes = [i32, i64, vp, vp]
+        L.orc_accumulator_restore.argtypes = [i32, i64, vp, vp]
         L.orc_reduce_each_microbatch.argtypes = [i32, i32, i64, i32, vp, f32, vp]
         L.orc_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32]
         L.orc_allgather.argtypes = [i32, i64, i32, vp, vp, i32]
@@ -177,6 +179,23 @@ def accumulate(acc: np.ndarray, g: np.ndarray, first: bool, finalize: bool, scal
     _check(lib().orc_accumulate(W, n, acc.ctypes.data, _dt(g), g.ctypes.data, int(first), int(finalize), scale,
                                 None if total is None else total.ctypes.data), "accumulate")
     return total
+
+
+def accumulator_save(acc: np.ndarray) -> np.ndarray:
+    """The reduced total a checkpoint holds: sum over replicas in rank order."""
+    assert acc.dtype == np.float32 and acc.flags.c_contiguous
+    W, n = acc.shape
+    total = np.empty(n, np.float32)
+    _check(lib().orc_accumulator_save(W, n, acc.ctypes.data, total.ctypes.data), "accumulator_save")
+    return total
+
+
+def accumulator_restore(total: np.ndarray, world: int) -> np.ndarray:
+    """The unreduced form of a total: replica 0 holds it, the others hold zero."""
+    t = np.ascontiguousarray(total, dtype=np.float32)
+    acc = np.empty((world, len(t)), np.float32)
+    _check(lib().orc_accumulator_restore(world, len(t), acc.ctypes.data, t.ctypes.data), "accumulator_restore")
+    return acc
 
 
 def reduce_each_microbatch(g: np.ndarray, scale: float = 1.0) -> np.ndarray:

@@ -458,3 +458,30 @@ void orc_bf16_to_f32_array(const uint16_t* in, float* out, int64_t n) {
 void orc_f32_to_bf16_array(const float* in, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_f32_to_bf16(in[i]);
 }
+
+/* --------------------------------------------- accumulator checkpoints --- */
+
+/* [MT] "What else had to change", "Accumulator lifetime": a checkpoint holds
+ * the reduced total, so saving runs the pending cross-replica all-reduce:
+ * total[k] = acc[0][k] + acc[1][k] + ... + acc[W-1][k] (rank order, fp32,
+ * from the rank-0 term).  acc is [world, n]; nothing is scaled. */
+int orc_accumulator_save(int world, int64_t n, const float* acc, float* total) {
+    if (world < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < n; ++k) {
+        float y = 0.0f;
+        for (int r = 0; r < world; ++r) y = (r == 0) ? acc[k] : y + acc[(int64_t)r * n + k];
+        total[k] = y;
+    }
+    return 0;
+}
+
+/* Same section: moving a reduced value back onto the unreduced form leaves
+ * the value on one replica and zeros on the rest, so the deferred all-reduce
+ * reproduces it: acc[0][k] = total[k], acc[r][k] = +0 for r > 0. */
+int orc_accumulator_restore(int world, int64_t n, float* acc, const float* total) {
+    if (world < 1 || n < 0) return -1;
+    for (int64_t k = 0; k < n; ++k) acc[k] = total[k];
+    for (int r = 1; r < world; ++r)
+        for (int64_t k = 0; k < n; ++k) acc[(int64_t)r * n + k] = 0.0f;
+    return 0;
+}

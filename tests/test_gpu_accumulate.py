@@ -95,3 +95,55 @@ def test_qwen3_full_size_sampled():
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
     per_mb = oracle.reduce_each_microbatch(gs).astype(np.float64)
     assert np.linalg.norm(got.astype(np.float64) - per_mb) / np.linalg.norm(per_mb) <= 5e-5
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_checkpoint_save_restore_bit_exact(world, offset):
+    n = 4096 * 3 + (0 if offset == 0 else 5)
+    store = torch.empty(world * n + offset, dtype=torch.float32, device="cuda")
+    acc = store[offset:].view(world, n)
+    datagen.fill_device(acc.data_ptr(), world, n, n, F32, NORMAL, 11, 0, 1, 0, 1e-3,
+                        torch.cuda.current_stream().cuda_stream)
+    tstore = torch.empty(n + offset, dtype=torch.float32, device="cuda")
+    total = tstore[offset:]
+    zc.accumulator_save(acc, total)
+    host_acc = datagen.host_matrix(world, n, F32, NORMAL, 11, sigma=1e-3)
+    want = oracle.accumulator_save(host_acc)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_bits(total), want.view(np.uint32))
+    zc.accumulator_restore(acc, total)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_bits(acc), oracle.accumulator_restore(want, world).view(np.uint32))
+
+
+def test_mid_step_checkpoint_round_trip_on_gpu():
+    """Accumulate 3 of 8 micro-batches, save, restore, finish: bit-identical to
+    the oracle doing the same, and within the reassociation tolerance of the
+    uninterrupted step."""
+    world, n, n_mb, cut = 4, 20000, 8, 3
+    s = torch.cuda.current_stream().cuda_stream
+    acc = torch.empty((world, n), dtype=torch.float32, device="cuda")
+    g = torch.empty((world, n), dtype=torch.float32, device="cuda")
+    total = torch.empty(n, dtype=torch.float32, device="cuda")
+    host_acc = np.empty((world, n), np.float32)
+    gs = []
+    for m in range(n_mb):
+        datagen.fill_device(g.data_ptr(), world, n, n, F32, NORMAL, 4, stream_id(0, m), 1, 0, 1e-3, s)
+        gh = datagen.host_matrix(world, n, F32, NORMAL, 4, stream0=stream_id(0, m), sigma=1e-3)
+        gs.append(gh)
+        last = m == n_mb - 1
+        zc.accumulate_microbatch(acc, g, first=(m == 0), finalize=last, total=total if last else None)
+        want = oracle.accumulate(host_acc, gh, first=(m == 0), finalize=last)
+        if m == cut - 1:
+            zc.accumulator_save(acc, total)
+            zc.accumulator_restore(acc, total)
+            host_acc = oracle.accumulator_restore(oracle.accumulator_save(host_acc), world)
+    torch.cuda.synchronize()
+    got = to_bits(total).view(np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    straight = np.empty((world, n), np.float32)
+    for m in range(n_mb):
+        ref = oracle.accumulate(straight, gs[m], first=(m == 0), finalize=(m == n_mb - 1))
+    d, r = got.astype(np.float64), ref.astype(np.float64)
+    assert np.linalg.norm(d - r) / np.linalg.norm(r) <= 5e-5

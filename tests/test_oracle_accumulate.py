@@ -98,3 +98,49 @@ def test_restore_form_reproduces_total():
     zeros = np.zeros((4, 3000), np.float32)
     out = oracle.accumulate(acc, zeros, first=False, finalize=True)
     assert np.array_equal(out, total)
+
+
+def test_checkpoint_restore_then_save_reproduces_total():
+    """PR #5099, "Accumulator lifetime": both directions are exact -- restoring
+    a total onto one replica with zeros elsewhere and reducing again gives the
+    total back (bit for bit, except that -0 becomes +0 once a +0 is added)."""
+    g = _grads(4, 3, 5000)
+    total = _deferred(g)
+    acc = oracle.accumulator_restore(total, 4)
+    assert np.array_equal(acc[0], total) and not acc[1:].any()
+    again = oracle.accumulator_save(acc)
+    assert np.array_equal(again.view(np.uint32), (total + np.float32(0)).view(np.uint32))
+
+
+def test_save_equals_finalize_with_zero_gradient():
+    g = _grads(4, 2, 4000)
+    acc = np.empty((4, 4000), np.float32)
+    oracle.accumulate(acc, g[0], True, False)
+    oracle.accumulate(acc, g[1], False, False)
+    saved = oracle.accumulator_save(acc)
+    fin = oracle.accumulate(acc.copy(), np.zeros_like(acc), False, True)
+    assert np.array_equal(saved, fin)   # x + 0 == x for every finite nonzero x, and the sums match
+    assert np.array_equal(saved, oracle.reduce_each_microbatch(acc[None]))
+
+
+@pytest.mark.parametrize("world,n_mb,cut", [(4, 8, 3), (2, 5, 1), (8, 4, 2)])
+def test_mid_step_round_trip_matches_uninterrupted_run(world, n_mb, cut):
+    """The mid-step checkpoint round trip of PR #5099's tests: exact on
+    integer-valued gradients (reassociation is exact there), within the
+    reassociation tolerance otherwise."""
+    rng = np.random.default_rng(world + n_mb)
+    gi = (rng.integers(-500, 500, size=(n_mb, world, 3000)) * 2.0 ** -9).astype(np.float32)
+    for g, exact in ((gi, True), (_grads(world, n_mb, 3000), False)):
+        straight = _deferred(g)
+        acc = np.empty((world, g.shape[2]), np.float32)
+        for m in range(cut):
+            oracle.accumulate(acc, g[m], m == 0, False)
+        acc = oracle.accumulator_restore(oracle.accumulator_save(acc), world)   # save, then restore
+        for m in range(cut, n_mb - 1):
+            oracle.accumulate(acc, g[m], False, False)
+        resumed = oracle.accumulate(acc, g[n_mb - 1], False, True)
+        if exact:
+            assert np.array_equal(resumed, straight)
+        else:
+            d, s = resumed.astype(np.float64), straight.astype(np.float64)
+            assert np.linalg.norm(d - s) / np.linalg.norm(s) <= 5e-5

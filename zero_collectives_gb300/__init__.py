@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
         L.dpred_flush_bucket_noalloc.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp,
                                                  vp]
         L.dpred_accumulate_microbatch.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp, vp]
+        L.dpred_accumulator_save.argtypes = [i32, i64, vp, vp, vp]
+        L.dpred_accumulator_restore.argtypes = [i32, i64, vp, vp, vp]
         L.dpred_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32, vp]
         L.dpred_allgather.argtypes = [i32, i64, i32, vp, vp, i32, vp]
         L.dpred_device_status.argtypes = [vp, i32]
@@ -294,6 +296,28 @@ def accumulate_microbatch(acc, g, first: bool, finalize: bool, scale: float = 1.
                                              int(finalize), float(scale),
                                              total.data_ptr() if finalize else None, _stream(stream)))
     return total
+
+
+def accumulator_save(acc, total, stream=None):
+    """total = sum over replica rows of acc (the reduced form a checkpoint holds)."""
+    import torch
+    if acc.dtype != torch.float32 or total.dtype != torch.float32 or not acc.is_contiguous() \
+            or total.numel() != acc.shape[1]:
+        raise ValueError("acc: contiguous fp32 [W, n]; total: fp32 [n]")
+    W, n = acc.shape
+    _check(lib().dpred_accumulator_save(W, n, acc.data_ptr(), total.data_ptr(), _stream(stream)))
+    return total
+
+
+def accumulator_restore(acc, total, stream=None):
+    """acc[0] = total, acc[1:] = 0 (the unreduced form of a restored total)."""
+    import torch
+    if acc.dtype != torch.float32 or total.dtype != torch.float32 or not acc.is_contiguous() \
+            or total.numel() != acc.shape[1]:
+        raise ValueError("acc: contiguous fp32 [W, n]; total: fp32 [n]")
+    W, n = acc.shape
+    _check(lib().dpred_accumulator_restore(W, n, acc.data_ptr(), total.data_ptr(), _stream(stream)))
+    return acc
 
 
 def reduce_scatter(inp, out, pre_div: bool = False, stream=None):

@@ -317,6 +317,25 @@ int dpred_accumulate_microbatch(int32_t world, int64_t n, float* acc, int32_t g_
                              static_cast<cudaStream_t>(stream));
 }
 
+static int check_acc_args(int32_t world, int64_t n, const float* acc, const float* total) {
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (n < 0) return set_error(DPRED_E_INVAL, "n < 0");
+    if (n > 0 && (!acc || !total)) return set_error(DPRED_E_INVAL, "null pointer");
+    if ((acc && !aligned(acc, 4)) || (total && !aligned(total, 4)))
+        return set_error(DPRED_E_ALIGN, "pointer not aligned to 4 bytes");
+    return DPRED_OK;
+}
+
+int dpred_accumulator_save(int32_t world, int64_t n, const float* acc, float* total, void* stream) {
+    int rc = check_acc_args(world, n, acc, total);
+    return rc ? rc : launch_accumulator_save(world, n, acc, total, static_cast<cudaStream_t>(stream));
+}
+
+int dpred_accumulator_restore(int32_t world, int64_t n, float* acc, const float* total, void* stream) {
+    int rc = check_acc_args(world, n, acc, total);
+    return rc ? rc : launch_accumulator_restore(world, n, acc, total, static_cast<cudaStream_t>(stream));
+}
+
 int dpred_reduce_scatter(int32_t n_nodes, int64_t m_elems, int32_t in_dtype, const void* in, int32_t out_dtype,
                          void* out, int32_t pre_div, void* stream) {
     if (n_nodes < 1 || n_nodes > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "n_nodes %d outside 1..%d", n_nodes, DPRED_MAX_WORLD);

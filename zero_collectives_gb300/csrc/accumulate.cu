@@ -209,7 +209,97 @@ int launch_typed(int world, int64_t n, float* acc, const Tg* g, int first, int f
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "accumulate kernel launch");
 }
 
+// Checkpoint form of the accumulator (MaxText PR #5099, "Accumulator
+// lifetime"): save reduces the replica rows to the total a checkpoint holds;
+// restore writes a total back as row 0 with zeros in the other rows.
+template <int W_T>
+__global__ void __launch_bounds__(kThreads) save_kernel(const float* __restrict__ acc, float* __restrict__ total,
+                                                        int world, int64_t n, int vec) {
+    const int W = W_T > 0 ? W_T : world;
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nv = n / 4;
+        const float4* a4 = reinterpret_cast<const float4*>(acc);
+        float4* t4 = reinterpret_cast<float4*>(total);
+        for (int64_t v = tid; v < nv; v += nthreads) {
+            float4 y = __ldcs(a4 + v);
+            if constexpr (W_T > 0) {
+                float4 q[W_T > 1 ? W_T - 1 : 1];
+#pragma unroll
+                for (int r = 1; r < W_T; ++r) q[r - 1] = __ldcs(a4 + r * nv + v);
+#pragma unroll
+                for (int r = 1; r < W_T; ++r)
+                    y = make_float4(__fadd_rn(y.x, q[r - 1].x), __fadd_rn(y.y, q[r - 1].y), __fadd_rn(y.z, q[r - 1].z),
+                                    __fadd_rn(y.w, q[r - 1].w));
+            } else {
+                for (int r = 1; r < W; ++r) {
+                    const float4 q = __ldcs(a4 + r * nv + v);
+                    y = make_float4(__fadd_rn(y.x, q.x), __fadd_rn(y.y, q.y), __fadd_rn(y.z, q.z), __fadd_rn(y.w, q.w));
+                }
+            }
+            __stcs(t4 + v, y);
+        }
+        done = nv * 4;
+    }
+    for (int64_t k = done + tid; k < n; k += nthreads) {
+        float y = acc[k];
+        for (int r = 1; r < W; ++r) y = __fadd_rn(y, acc[(int64_t)r * n + k]);
+        total[k] = y;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) restore_kernel(float* __restrict__ acc, const float* __restrict__ total,
+                                                           int world, int64_t n, int vec) {
+    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int64_t nthreads = (int64_t)gridDim.x * kThreads;
+    if (vec) {
+        const int64_t nv = n / 4, all = (int64_t)world * nv;
+        float4* a4 = reinterpret_cast<float4*>(acc);
+        const float4* t4 = reinterpret_cast<const float4*>(total);
+        for (int64_t i = tid; i < all; i += nthreads)
+            __stcs(a4 + i, i < nv ? __ldcs(t4 + i) : make_float4(0.f, 0.f, 0.f, 0.f));
+        return;
+    }
+    const int64_t all = (int64_t)world * n;
+    for (int64_t i = tid; i < all; i += nthreads) acc[i] = i < n ? total[i] : 0.0f;
+}
+
 }  // namespace
+
+int launch_accumulator_save(int world, int64_t n, const float* acc, float* total, cudaStream_t s) {
+    if ((int64_t)world * n == 0) return DPRED_OK;
+    const int vec = reinterpret_cast<uintptr_t>(acc) % 16 == 0 && reinterpret_cast<uintptr_t>(total) % 16 == 0 &&
+                    n % 4 == 0;
+    const int64_t items = vec ? n / 4 : n;
+#define DPRED_SAVE(WT)                                                             \
+    {                                                                              \
+        auto k = save_kernel<WT>;                                                  \
+        k<<<grid_for(k, items), kThreads, 0, s>>>(acc, total, world, n, vec);      \
+        break;                                                                     \
+    }
+    switch (world) {
+        case 1: DPRED_SAVE(1)
+        case 2: DPRED_SAVE(2)
+        case 4: DPRED_SAVE(4)
+        case 8: DPRED_SAVE(8)
+        default: DPRED_SAVE(0)
+    }
+#undef DPRED_SAVE
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DPRED_OK : cuda_error(e, "accumulator save launch");
+}
+
+int launch_accumulator_restore(int world, int64_t n, float* acc, const float* total, cudaStream_t s) {
+    if ((int64_t)world * n == 0) return DPRED_OK;
+    const int vec = reinterpret_cast<uintptr_t>(acc) % 16 == 0 && reinterpret_cast<uintptr_t>(total) % 16 == 0 &&
+                    n % 4 == 0;
+    const int64_t items = vec ? (int64_t)world * n / 4 : (int64_t)world * n;
+    restore_kernel<<<grid_for(restore_kernel, items), kThreads, 0, s>>>(acc, total, world, n, vec);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? DPRED_OK : cuda_error(e, "accumulator restore launch");
+}
 
 int launch_accumulate(int world, int64_t n, float* acc, int g_dt, const void* g, int first, int finalize, float scale,
                       float* total, cudaStream_t s) {

@@ -126,6 +126,9 @@ int launch_flush_f32_in(const FlushLaunch& L, cudaStream_t s);
 int launch_accumulate(int world, int64_t n, float* acc, int g_dt, const void* g, int first, int finalize,
                       float scale, float* total, cudaStream_t s);
 
+int launch_accumulator_save(int world, int64_t n, const float* acc, float* total, cudaStream_t s);
+int launch_accumulator_restore(int world, int64_t n, float* acc, const float* total, cudaStream_t s);
+
 int launch_allgather(int n_nodes, int64_t shard_elems, int esize, const void* in, void* out, int order,
                      cudaStream_t s);
 
