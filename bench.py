@@ -443,7 +443,39 @@ def rows(peak):
         ms = timed(f, 5)
         writes = sum(int(tree.numel[p]) * (1 if om.owner[p] >= 0 else WORLD) for p in range(tree.n_params))
         out[name] = entry(ms, WORLD * n * 2 + writes * 2, workload="402.8M W=8 bf16, 7 buckets, in place")
-    del g
+
+    # Partitioned flush (every rank gets exactly its partition slice) over the
+    # 7 arrival-order buckets, and over the whole model as one bucket against
+    # the two-pass relayout + ReduceScatter that ncclReduceScatter would need.
+    flat = np.concatenate([[0], np.cumsum(tree.numel)[:-1]]).astype(np.int64)
+    P = -(-n // WORLD)
+    parts = [torch.empty(P, dtype=torch.bfloat16, device="cuda") for _ in range(WORLD)]
+    wsf = torch.empty(zc.flush_workspace_bytes(WORLD, tree.n_params + WORLD), dtype=torch.uint8, device="cuda")
+
+    def part7():
+        for b in layout.buckets:
+            zc.flush_bucket_partitioned(g[:, b.start:b.start + b.size], b.tasks, flat, P, parts, zc.BF16, True,
+                                        workspace=wsf)
+
+    ms = timed(part7, 5)
+    out["flush_partitioned_step"] = entry(ms, WORLD * n * 2 + n * 2,
+                                          workload="402.8M W=8 bf16, 7 buckets, each rank its partition slice")
+    one = workloads.arrival_layout(tree, capacity=None).buckets[0]
+    ms = timed(lambda: zc.flush_bucket_partitioned(g, one.tasks, flat, P, parts, zc.BF16, True, workspace=wsf), 5)
+    out["flush_partitioned_one_bucket"] = entry(ms, WORLD * n * 2 + n * 2, workload="402.8M W=8 bf16 as one bucket")
+    relaid = torch.empty((WORLD, WORLD * P), dtype=torch.bfloat16, device="cuda")
+    rs_out = torch.empty((WORLD, P), dtype=torch.bfloat16, device="cuda")
+    wsr = torch.empty(zc.bucket_relayout_workspace_bytes(WORLD, len(one.tasks)), dtype=torch.uint8, device="cuda")
+
+    def two_pass():
+        zc.bucket_relayout(g, one.tasks, flat, P, P, relaid, workspace=wsr)
+        zc.reduce_scatter(relaid, rs_out, pre_div=True)
+
+    ms = timed(two_pass, 5)
+    out["relayout_then_reduce_scatter_one_bucket"] = entry(
+        ms, 2 * WORLD * n * 2 + WORLD * WORLD * P * 2 + WORLD * P * 2,
+        workload="402.8M W=8 bf16 as one bucket: relayout pass + ReduceScatter", launches=2)
+    del g, parts, relaid, rs_out
 
     # Deferred accumulation: W=4, 8 micro-batches, qwen3-0.6b tree, fp32.
     W, M = 4, 8

@@ -206,6 +206,57 @@ int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int
                                dpred_probe* probe, void* stream);
 
 /*
+ * Partitioned flush: every rank receives exactly its optimizer partition's
+ * slice of the reduced bucket.  [DS] "Describe alternatives you've considered"
+ * (ncclReduceScatter over the bucket, "the better end state", same traffic
+ * class as reduce-to-owner) and "Follow-up" (ZeRO-2 registers real buffers
+ * with offsets, so the destination is a slice of the rank's partition, not a
+ * full-parameter buffer).  Here it is one fused pass over the arrival-order
+ * bucket; no relayout is needed.
+ *
+ * grads, ld, tasks, pre_div: as for dpred_flush_bucket.  flat_offset (host,
+ * [n_params]) is each parameter's start in its group's flat space;
+ * part_size = ceil(T / world) elements per partition.  Element k of task t
+ * (flat position f = flat_offset[param_id] + k) is reduced and written to
+ * part_dst[r][f - r * part_size] with r = f / part_size; part_dst (host,
+ * [world]) holds device pointers to the ranks' partition buffers (part_size
+ * elements of out_dtype; NULL = that rank receives nothing).  A parameter
+ * straddling a boundary is split there: each holder receives only its own
+ * slice.  probe (may be NULL): tasks, reduced_elems, owner_tasks/owner_elems
+ * = tasks lying inside one partition, kept_elems[r] = elements delivered to
+ * rank r.  Workspace: dpred_flush_workspace_bytes(world, n_tasks + world - 1)
+ * bytes suffice.  Errors: DPRED_E_INVAL, DPRED_E_ALIGN, DPRED_E_SIZE (a task
+ * outside the row or the world's partitions, overlapping tasks, workspace too
+ * small), DPRED_E_CUDA.  Asynchronous on `stream`.
+ */
+int dpred_flush_bucket_partitioned(int32_t world, int32_t in_dtype, const void* grads, int64_t ld,
+                                   const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset,
+                                   int32_t n_params, int64_t part_size, int32_t out_dtype, void* const* part_dst,
+                                   int32_t pre_div, dpred_probe* probe, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/*
+ * Bucket relayout pass: the copy that ncclReduceScatter over an arrival-order
+ * bucket needs first ([DS] "Describe alternatives you've considered").  Every
+ * replica row q of grads is rewritten rank-major into out (device,
+ * [world, out_ld], out_ld >= world * seg): out[q][r * seg + j] = the j-th
+ * element, in flat order, of the bucket's elements that lie in partition r.
+ * seg_used (host, [world]) receives each run's length; out elements past a
+ * run are not written.  dpred_reduce_scatter(world, world * seg, ...) of out
+ * then gives rank r its reduced run, identical to what
+ * dpred_flush_bucket_partitioned writes.  Arguments as for the partitioned
+ * flush; the bucket's elements within one partition must form one contiguous
+ * flat run (true for whole-parameter buckets of consecutive parameters).  A
+ * pure byte copy.  Workspace: dpred_bucket_relayout_workspace_bytes(world,
+ * n_tasks).  Asynchronous on `stream`.
+ */
+size_t dpred_bucket_relayout_workspace_bytes(int32_t world, int32_t n_tasks);
+int dpred_bucket_relayout(int32_t world, int32_t dtype, const void* grads, int64_t ld, const dpred_task* tasks,
+                          int32_t n_tasks, const int64_t* flat_offset, int32_t n_params, int64_t part_size, int64_t seg,
+                          void* out, int64_t out_ld, int64_t* seg_used, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/*
  * Replica-local gradient accumulation with one cross-replica reduction per
  * optimizer step.  [MT] "What" (cotangents come out unreduced, a per-replica
  * partial sum that accumulates replica-locally across micro-batches; update()

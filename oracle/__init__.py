@@ -40,6 +40,8 @@ def lib():
         L.orc_owner_map.argtypes = [i32, i32, i32, vp, vp, vp, vp, i32, vp, vp, vp, vp, vp]
         L.orc_flush.argtypes = [i32, i32, vp, i64, i32, vp, vp, vp, vp, i32, i32, vp, i32, i32, vp]
         L.orc_flush_probe.argtypes = [i32, i32, vp, vp, vp, i32, vp, i32, vp]
+        L.orc_flush_partitioned.argtypes = [i32, i32, vp, i64, i32, vp, vp, vp, vp, i64, i32, vp, i32, vp]
+        L.orc_bucket_relayout.argtypes = [i32, i32, vp, i64, i32, vp, vp, vp, vp, i64, i64, vp, i64, vp]
         L.orc_accumulate.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp]
         L.orc_accumulator_save.argtypes = [i32, i64, vp, vp]
         L.orc_accumulator_restore.argtypes = [i32, i64, vp, vp]
@@ -168,6 +170,44 @@ def flush_probe(world: int, tasks: np.ndarray, owner: np.ndarray | None, n_param
                                  None if has is None else has.ctypes.data, int(reduce_to_owner), probe.ctypes.data),
            "flush_probe")
     return _probe_dict(probe)
+
+
+def flush_partitioned(world: int, grads: np.ndarray, tasks: np.ndarray, flat_offset: np.ndarray, part_size: int,
+                      part_dst: list, out_dt: int, pre_div: bool = True) -> dict:
+    """Every rank receives its partition's slice of the reduced bucket
+    (part_dst[r]: numpy array of part_size elements, or None)."""
+    assert grads.flags.c_contiguous
+    W, ld = grads.shape
+    tp = np.ascontiguousarray(tasks["param_id"], dtype=np.int32)
+    to = np.ascontiguousarray(tasks["offset"], dtype=np.int64)
+    tn = np.ascontiguousarray(tasks["numel"], dtype=np.int64)
+    fo = np.ascontiguousarray(flat_offset, dtype=np.int64)
+    table = (ctypes.c_void_p * world)()
+    for r in range(world):
+        if part_dst[r] is not None:
+            assert part_dst[r].dtype == _np_dtype(out_dt) and part_dst[r].size >= part_size
+            table[r] = part_dst[r].ctypes.data
+    probe = np.zeros(4 + world, dtype=np.int64)
+    _check(lib().orc_flush_partitioned(world, _dt(grads), grads.ctypes.data, ld, len(tasks), tp.ctypes.data,
+                                       to.ctypes.data, tn.ctypes.data, fo.ctypes.data, part_size, out_dt, table,
+                                       int(pre_div), probe.ctypes.data), "flush_partitioned")
+    return _probe_dict(probe)
+
+
+def bucket_relayout(grads: np.ndarray, tasks: np.ndarray, flat_offset: np.ndarray, part_size: int, seg: int,
+                    out: np.ndarray) -> np.ndarray:
+    """Rank-major relayout of a bucket into out ([W, >= W*seg]); returns seg_used."""
+    assert grads.flags.c_contiguous and out.flags.c_contiguous and out.dtype == grads.dtype
+    W, ld = grads.shape
+    tp = np.ascontiguousarray(tasks["param_id"], dtype=np.int32)
+    to = np.ascontiguousarray(tasks["offset"], dtype=np.int64)
+    tn = np.ascontiguousarray(tasks["numel"], dtype=np.int64)
+    fo = np.ascontiguousarray(flat_offset, dtype=np.int64)
+    used = np.zeros(W, np.int64)
+    _check(lib().orc_bucket_relayout(W, grads.dtype.itemsize, grads.ctypes.data, ld, len(tasks), tp.ctypes.data,
+                                     to.ctypes.data, tn.ctypes.data, fo.ctypes.data, part_size, seg, out.ctypes.data,
+                                     out.shape[1], used.ctypes.data), "bucket_relayout")
+    return used
 
 
 def accumulate(acc: np.ndarray, g: np.ndarray, first: bool, finalize: bool, scale: float = 1.0):

@@ -485,3 +485,99 @@ int orc_accumulator_restore(int world, int64_t n, float* acc, const float* total
         for (int64_t k = 0; k < n; ++k) acc[(int64_t)r * n + k] = 0.0f;
     return 0;
 }
+
+/* ------------------------------------- partitioned (ReduceScatter) flush --- */
+
+/* [DS] "Describe alternatives you've considered", ncclReduceScatter over the
+ * bucket ("the better end state"), and "Follow-up" (ZeRO-2 registers real
+ * buffers with offsets): every rank receives exactly the part of the reduced
+ * bucket that lies in its optimizer partition.  Element k of task t belongs
+ * to flat position f = flat_offset[param] + k of its group; it goes to rank
+ * r = f / part_size at position f - r * part_size of that rank's partition
+ * buffer part_dst[r] (NULL: the rank receives nothing).  The value is the
+ * same element reduction as the flush.  probe (may be NULL): [0] tasks,
+ * [1] reduced_elems, [2] tasks lying inside one partition, [3] their
+ * elements, [4 + r] elements delivered to rank r. */
+int orc_flush_partitioned(int world, int in_dt, const void* grads, int64_t ld, int n_tasks, const int32_t* task_param,
+                          const int64_t* task_off, const int64_t* task_numel, const int64_t* flat_offset,
+                          int64_t part_size, int out_dt, void* const* part_dst, int pre_div, int64_t* probe) {
+    if (world < 1 || !dtype_ok(in_dt) || !dtype_ok(out_dt) || n_tasks < 0 || part_size < 1) return -1;
+    for (int t = 0; t < n_tasks; ++t) {
+        if (task_off[t] < 0 || task_numel[t] < 0 || task_off[t] + task_numel[t] > ld) return -1;
+        int64_t s = flat_offset[task_param[t]];
+        if (s < 0 || (task_numel[t] > 0 && (s + task_numel[t] - 1) / part_size >= world)) return -1;
+    }
+    if (probe) {
+        probe[0] = n_tasks;
+        probe[1] = probe[2] = probe[3] = 0;
+        for (int r = 0; r < world; ++r) probe[4 + r] = 0;
+    }
+    for (int t = 0; t < n_tasks; ++t) {
+        const int64_t s = flat_offset[task_param[t]];
+        for (int64_t k = 0; k < task_numel[t]; ++k) {
+            const int64_t f = s + k;
+            const int r = (int)(f / part_size);
+            const float y = reduce_one(world, in_dt, grads, ld, task_off[t] + k, pre_div);
+            if (part_dst[r] != NULL) {
+                store_elem(out_dt, part_dst[r], f - (int64_t)r * part_size, y);
+                if (probe) probe[4 + r] += 1;
+            }
+        }
+        if (probe) {
+            probe[1] += task_numel[t];
+            if (task_numel[t] > 0 && s / part_size == (s + task_numel[t] - 1) / part_size) {
+                probe[2] += 1;
+                probe[3] += task_numel[t];
+            }
+        }
+    }
+    return 0;
+}
+
+/* The relayout pass of [DS] "Describe alternatives you've considered": the
+ * bucket, in gradient-arrival order, is rewritten so that every replica row
+ * holds the elements bound for rank 0, then those for rank 1, ..., each
+ * rank's run in flat order and padded to `seg` elements: out[q][r * seg + j]
+ * is the j-th element (in flat order) of the bucket that lies in partition r,
+ * taken from replica row q.  ReduceScatter of out over the W rows then
+ * delivers to rank r the reduced run r.  seg_used[r] receives the run
+ * lengths; elements past them are not written.  A plain copy. */
+int orc_bucket_relayout(int world, int esize, const void* grads, int64_t ld, int n_tasks, const int32_t* task_param,
+                        const int64_t* task_off, const int64_t* task_numel, const int64_t* flat_offset,
+                        int64_t part_size, int64_t seg, void* out, int64_t out_ld, int64_t* seg_used) {
+    if (world < 1 || esize < 1 || n_tasks < 0 || part_size < 1 || seg < 0) return -1;
+    /* run start of every rank = smallest flat position of the bucket in that partition */
+    int64_t* first = (int64_t*)malloc(sizeof(int64_t) * (size_t)world);
+    if (!first) return -1;
+    for (int r = 0; r < world; ++r) {
+        first[r] = -1;
+        seg_used[r] = 0;
+    }
+    for (int t = 0; t < n_tasks; ++t) {
+        const int64_t s = flat_offset[task_param[t]];
+        for (int64_t k = 0; k < task_numel[t]; ++k) {
+            const int64_t f = s + k;
+            const int r = (int)(f / part_size);
+            if (r >= world) { free(first); return -1; }
+            if (first[r] < 0 || f < first[r]) first[r] = f;
+            seg_used[r] += 1;
+        }
+    }
+    for (int r = 0; r < world; ++r)
+        if (seg_used[r] > seg) { free(first); return -3; }
+    /* the bucket's elements in one partition must be one contiguous flat run */
+    for (int t = 0; t < n_tasks; ++t) {
+        const int64_t s = flat_offset[task_param[t]];
+        for (int64_t k = 0; k < task_numel[t]; ++k) {
+            const int64_t f = s + k;
+            const int r = (int)(f / part_size);
+            const int64_t j = f - first[r];
+            if (j >= seg_used[r]) { free(first); return -1; }
+            for (int q = 0; q < world; ++q)
+                memcpy((char*)out + ((int64_t)q * out_ld + (int64_t)r * seg + j) * esize,
+                       (const char*)grads + ((int64_t)q * ld + task_off[t] + k) * esize, (size_t)esize);
+        }
+    }
+    free(first);
+    return 0;
+}

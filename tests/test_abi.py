@@ -196,3 +196,27 @@ def test_owner_map_argument_errors(L):
     n[1] = -3
     assert L.dpred_build_owner_map(2, 0, g, 1, 1, own.ctypes.data, own.ctypes.data, own.ctypes.data,
                                    ctypes.byref(a), ctypes.byref(b)) == -1
+
+
+def test_partitioned_and_relayout_validation(L):
+    tasks = _tasks([(0, 0, 10), (1, 10, 10)])
+    flat = np.array([0, 10], np.int64)
+    tbl = (ctypes.c_void_p * 2)(0x20000, 0x30000)
+    used = np.zeros(2, np.int64)
+    # a flat range beyond the world's partitions
+    assert L.dpred_flush_bucket_partitioned(2, 0, 0x10000, 100, tasks.ctypes.data, 2, flat.ctypes.data, 2, 5, 0, tbl,
+                                            1, None, None, 0, None) == -3
+    # param id outside the offset table
+    assert L.dpred_flush_bucket_partitioned(2, 0, 0x10000, 100, tasks.ctypes.data, 2, flat.ctypes.data, 1, 10, 0, tbl,
+                                            1, None, None, 0, None) == -1
+    # overlapping flat ranges
+    bad = np.array([0, 5], np.int64)
+    assert L.dpred_flush_bucket_partitioned(2, 0, 0x10000, 100, tasks.ctypes.data, 2, bad.ctypes.data, 2, 10, 0, tbl,
+                                            1, None, None, 0, None) == -3
+    # relayout: seg too small for a rank's run
+    assert L.dpred_bucket_relayout(2, 0, 0x10000, 100, tasks.ctypes.data, 2, flat.ctypes.data, 2, 10, 5, 0x40000, 10,
+                                   used.ctypes.data, None, 0, None) == -3
+    # relayout: a partition's elements that are not one flat run
+    gap = np.array([0, 12], np.int64)
+    assert L.dpred_bucket_relayout(2, 0, 0x10000, 100, tasks.ctypes.data, 2, gap.ctypes.data, 2, 30, 30, 0x40000, 60,
+                                   used.ctypes.data, None, 0, None) == -1

@@ -68,6 +68,12 @@ def lib() -> ctypes.CDLL:
         L.dpred_flush_bucket_noalloc.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp,
                                                  vp]
         L.dpred_accumulate_microbatch.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp, vp]
+        L.dpred_flush_bucket_partitioned.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i64, i32, vp, i32, vp, vp,
+                                                     ctypes.c_size_t, vp]
+        L.dpred_bucket_relayout_workspace_bytes.restype = ctypes.c_size_t
+        L.dpred_bucket_relayout_workspace_bytes.argtypes = [i32, i32]
+        L.dpred_bucket_relayout.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i64, i64, vp, i64, vp, vp,
+                                            ctypes.c_size_t, vp]
         L.dpred_accumulator_save.argtypes = [i32, i64, vp, vp, vp]
         L.dpred_accumulator_restore.argtypes = [i32, i64, vp, vp, vp]
         L.dpred_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32, vp]
@@ -280,6 +286,52 @@ def flush_bucket_noalloc(grads, tasks: np.ndarray, owner, dst: DstTable | None, 
                                             None if dst is None else dst.c, int(pre_div), int(reduce_to_owner),
                                             int(checked), None if p is None else ctypes.byref(p), _stream(stream)))
     return _probe_from(p, world) if p is not None else None
+
+
+def flush_bucket_partitioned(grads, tasks: np.ndarray, flat_offset, part_size: int, part_dst, out_dtype: int | None = None,
+                             pre_div: bool = True, probe: bool = False, workspace=None, stream=None):
+    """Every rank gets its partition's slice of the reduced bucket.  part_dst:
+    list of CUDA tensors (each >= part_size elements) or None per rank."""
+    if grads.dim() != 2 or grads.stride(1) != 1:
+        raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
+    world = grads.shape[0]
+    in_dt = _dtype_code(grads)
+    out_dt = in_dt if out_dtype is None else out_dtype
+    ld = grads.stride(0) if world > 1 else grads.shape[1]
+    t = _tasks_arg(tasks)
+    fo = np.ascontiguousarray(flat_offset, dtype=np.int64)
+    table = (ctypes.c_void_p * world)(*[None if d is None else d.data_ptr() for d in part_dst])
+    p = _Probe() if probe else None
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                             workspace.numel() * workspace.element_size())
+    _check(lib().dpred_flush_bucket_partitioned(world, in_dt, grads.data_ptr(), ld, t.ctypes.data, len(t),
+                                                fo.ctypes.data, len(fo), int(part_size), out_dt, table, int(pre_div),
+                                                None if p is None else ctypes.byref(p), ws_ptr, ws_bytes,
+                                                _stream(stream)))
+    return _probe_from(p, world) if p is not None else None
+
+
+def bucket_relayout(grads, tasks: np.ndarray, flat_offset, part_size: int, seg: int, out, workspace=None,
+                    stream=None) -> np.ndarray:
+    """Rank-major relayout of the bucket into out ([W, >= W*seg]); returns the run lengths."""
+    if grads.dim() != 2 or grads.stride(1) != 1 or out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("2-D CUDA tensors with unit column stride required")
+    world = grads.shape[0]
+    t = _tasks_arg(tasks)
+    fo = np.ascontiguousarray(flat_offset, dtype=np.int64)
+    used = np.zeros(world, np.int64)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                             workspace.numel() * workspace.element_size())
+    _check(lib().dpred_bucket_relayout(world, _dtype_code(grads), grads.data_ptr(),
+                                       grads.stride(0) if world > 1 else grads.shape[1], t.ctypes.data, len(t),
+                                       fo.ctypes.data, len(fo), int(part_size), int(seg), out.data_ptr(),
+                                       out.stride(0) if world > 1 else out.shape[1], used.ctypes.data, ws_ptr,
+                                       ws_bytes, _stream(stream)))
+    return used
+
+
+def bucket_relayout_workspace_bytes(world: int, n_tasks: int) -> int:
+    return int(lib().dpred_bucket_relayout_workspace_bytes(world, n_tasks))
 
 
 # ----------------------------------------------------- accumulate / RS / AG ---

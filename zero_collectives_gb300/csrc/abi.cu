@@ -317,6 +317,132 @@ int dpred_accumulate_microbatch(int32_t world, int64_t n, float* acc, int32_t g_
                              static_cast<cudaStream_t>(stream));
 }
 
+// Pieces of a bucket cut at partition boundaries: {task, rank, flat lo, flat hi}.
+struct PartPiece {
+    int task, rank;
+    int64_t lo, hi;
+};
+
+static int partition_pieces(int32_t world, const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset,
+                            int32_t n_params, int64_t part_size, std::vector<PartPiece>& out) {
+    if (!flat_offset && n_tasks > 0) return set_error(DPRED_E_INVAL, "null flat_offset");
+    if (part_size < 1) return set_error(DPRED_E_INVAL, "part_size < 1");
+    for (int t = 0; t < n_tasks; ++t) {
+        const dpred_task& k = tasks[t];
+        if (k.param_id < 0 || k.param_id >= n_params)
+            return set_error(DPRED_E_INVAL, "task %d: param_id %d outside 0..%d", t, k.param_id, n_params - 1);
+        if (k.numel == 0) continue;
+        const int64_t s = flat_offset[k.param_id], e = s + k.numel;
+        if (s < 0 || (e - 1) / part_size >= world)
+            return set_error(DPRED_E_SIZE, "task %d: flat range [%lld, %lld) outside %d partitions of %lld", t,
+                             (long long)s, (long long)e, world, (long long)part_size);
+        for (int64_t r = s / part_size; r <= (e - 1) / part_size; ++r)
+            out.push_back(PartPiece{t, (int)r, std::max(s, r * part_size), std::min(e, (r + 1) * part_size)});
+    }
+    std::vector<std::pair<int64_t, int64_t>> ranges;
+    for (const PartPiece& p : out) ranges.emplace_back(p.lo, p.hi);
+    std::sort(ranges.begin(), ranges.end());
+    for (size_t i = 1; i < ranges.size(); ++i)
+        if (ranges[i].first < ranges[i - 1].second) return set_error(DPRED_E_SIZE, "tasks overlap in the flat space");
+    return DPRED_OK;
+}
+
+int dpred_flush_bucket_partitioned(int32_t world, int32_t in_dtype, const void* grads, int64_t ld,
+                                   const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset,
+                                   int32_t n_params, int64_t part_size, int32_t out_dtype, void* const* part_dst,
+                                   int32_t pre_div, dpred_probe* probe, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    if (ld < 0) return set_error(DPRED_E_INVAL, "ld < 0");
+    int rc = validate_tasks(world, tasks, n_tasks, nullptr, 0, ld, true);
+    if (rc) return rc;
+    if (n_tasks > 0 && !part_dst) return set_error(DPRED_E_INVAL, "null part_dst table");
+    const int isz = elem_size(in_dtype), osz = elem_size(out_dtype);
+    bool any = false;
+    for (int t = 0; t < n_tasks; ++t) any |= tasks[t].numel > 0;
+    if (any && !grads) return set_error(DPRED_E_INVAL, "null grads");
+    if (grads && !aligned(grads, isz)) return set_error(DPRED_E_ALIGN, "grads not aligned to its element size");
+    for (int r = 0; r < world && part_dst; ++r)
+        if (part_dst[r] && !aligned(part_dst[r], osz)) return set_error(DPRED_E_ALIGN, "partition %d misaligned", r);
+    std::vector<PartPiece> pieces;
+    rc = partition_pieces(world, tasks, n_tasks, flat_offset, n_params, part_size, pieces);
+    if (rc) return rc;
+    if (probe) {
+        probe->tasks = n_tasks;
+        probe->reduced_elems = probe->owner_tasks = probe->owner_elems = 0;
+        for (int r = 0; r < DPRED_MAX_WORLD; ++r) probe->kept_elems[r] = 0;
+        for (int t = 0; t < n_tasks; ++t) {
+            probe->reduced_elems += tasks[t].numel;
+            if (tasks[t].numel == 0) continue;
+            const int64_t s = flat_offset[tasks[t].param_id];
+            if (s / part_size == (s + tasks[t].numel - 1) / part_size) {
+                probe->owner_tasks += 1;
+                probe->owner_elems += tasks[t].numel;
+            }
+        }
+        for (const PartPiece& p : pieces)
+            if (part_dst[p.rank]) probe->kept_elems[p.rank] += p.hi - p.lo;
+    }
+    std::vector<Dest> plan;
+    plan.reserve(pieces.size());
+    for (const PartPiece& p : pieces) {
+        if (!part_dst[p.rank]) continue;
+        Dest d;
+        d.src_off = tasks[p.task].offset + (p.lo - flat_offset[tasks[p.task].param_id]);
+        d.numel = p.hi - p.lo;
+        d.ptrs.push_back(static_cast<char*>(part_dst[p.rank]) + (p.lo - p.rank * part_size) * osz);
+        plan.push_back(std::move(d));
+    }
+    return run_plan(world, in_dtype, grads, ld, out_dtype, pre_div, plan, workspace, workspace_bytes,
+                    static_cast<cudaStream_t>(stream));
+}
+
+size_t dpred_bucket_relayout_workspace_bytes(int32_t world, int32_t n_tasks) {
+    if (world < 1 || n_tasks < 0) return 0;
+    return relayout_workspace_bytes((int64_t)world * ((int64_t)n_tasks + world - 1));
+}
+
+int dpred_bucket_relayout(int32_t world, int32_t dtype, const void* grads, int64_t ld, const dpred_task* tasks,
+                          int32_t n_tasks, const int64_t* flat_offset, int32_t n_params, int64_t part_size, int64_t seg,
+                          void* out, int64_t out_ld, int64_t* seg_used, void* workspace, size_t workspace_bytes,
+                          void* stream) {
+    if (!dtype_ok(dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    if (ld < 0 || seg < 0 || out_ld < (int64_t)world * seg) return set_error(DPRED_E_INVAL, "bad ld / seg / out_ld");
+    if (!seg_used) return set_error(DPRED_E_INVAL, "null seg_used");
+    int rc = validate_tasks(world, tasks, n_tasks, nullptr, 0, ld, true);
+    if (rc) return rc;
+    const int esz = elem_size(dtype);
+    if ((grads && !aligned(grads, esz)) || (out && !aligned(out, esz)))
+        return set_error(DPRED_E_ALIGN, "pointer not aligned to its element size");
+    std::vector<PartPiece> pieces;
+    rc = partition_pieces(world, tasks, n_tasks, flat_offset, n_params, part_size, pieces);
+    if (rc) return rc;
+    std::vector<int64_t> first(world, -1);
+    for (int r = 0; r < world; ++r) seg_used[r] = 0;
+    for (const PartPiece& p : pieces) {
+        if (first[p.rank] < 0 || p.lo < first[p.rank]) first[p.rank] = p.lo;
+        seg_used[p.rank] += p.hi - p.lo;
+    }
+    for (int r = 0; r < world; ++r)
+        if (seg_used[r] > seg) return set_error(DPRED_E_SIZE, "rank %d needs %lld elements, seg is %lld", r,
+                                                (long long)seg_used[r], (long long)seg);
+    for (const PartPiece& p : pieces)
+        if (p.hi - first[p.rank] > seg_used[p.rank])
+            return set_error(DPRED_E_INVAL, "the bucket's elements in partition %d are not one contiguous flat run", p.rank);
+    if (!pieces.empty() && (!grads || !out)) return set_error(DPRED_E_INVAL, "null pointer");
+    std::vector<int64_t> triples;
+    triples.reserve(pieces.size() * world * 3);
+    for (int q = 0; q < world; ++q)
+        for (const PartPiece& p : pieces) {
+            const dpred_task& k = tasks[p.task];
+            triples.push_back(((int64_t)q * ld + k.offset + (p.lo - flat_offset[k.param_id])) * esz);
+            triples.push_back(((int64_t)q * out_ld + (int64_t)p.rank * seg + (p.lo - first[p.rank])) * esz);
+            triples.push_back((p.hi - p.lo) * esz);
+        }
+    return launch_copy_plan(static_cast<const char*>(grads), static_cast<char*>(out), triples, workspace,
+                            workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
 static int check_acc_args(int32_t world, int64_t n, const float* acc, const float* total) {
     if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
     if (n < 0) return set_error(DPRED_E_INVAL, "n < 0");

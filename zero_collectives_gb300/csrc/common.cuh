@@ -12,6 +12,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "dpred.h"
 
 namespace dpred {
@@ -131,6 +133,11 @@ int launch_accumulator_restore(int world, int64_t n, float* acc, const float* to
 
 int launch_allgather(int n_nodes, int64_t shard_elems, int esize, const void* in, void* out, int order,
                      cudaStream_t s);
+
+// Plan-driven byte copy (the relayout pass): triples of {src byte offset, dst byte offset, bytes}.
+int launch_copy_plan(const char* src, char* dst, const std::vector<int64_t>& triples, void* workspace,
+                     size_t workspace_bytes, cudaStream_t s);
+size_t relayout_workspace_bytes(int64_t n_pieces);
 
 int* device_error_word();  // device address of the error word (current device)
 
