@@ -340,6 +340,37 @@ int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const v
 int dpred_set_flush_path(int32_t path);
 
 /*
+ * AllGather schedules, executed step by step.  [AG] "Ring AllGather" (N-1
+ * steps; in step s every node forwards to its right neighbour the chunk it
+ * received in step s-1), the bidirectional ring (eq. ag-bidir-ring:
+ * ceil((N-1)/2) steps; in step s node i receives chunk i-s from its left and
+ * chunk i+s from its right neighbour) and "Recursive Doubling AllGather"
+ * (N = 2^k; log2 N steps; in step j node i receives everything node
+ * i xor 2^(j-1) holds).  The N node buffers are the rows of bufs (device,
+ * [N, N * shard_elems]); slot c of row i holds one shard.  Layouts: ring
+ * lists in ring order (slot c of node i = A_{(i-c) mod N}, as the page's N=4
+ * table and dpred_allgather order 1); bidirectional ring and recursive
+ * doubling keep every chunk at its own index (order 0).
+ *   dpred_allgather_schedule_steps: the number of steps, or DPRED_E_INVAL.
+ *   dpred_allgather_schedule_init:  copies shard i of in ([N, shard_elems])
+ *                                   into node i's first slot (ring) or slot i.
+ *   dpred_allgather_schedule_step:  one step (1 <= step <= steps): one kernel
+ *                                   launch moving exactly the chunks that the
+ *                                   schedule sends in that step; slots a node
+ *                                   does not yet hold are never written.
+ * A bit copy.  Errors: DPRED_E_INVAL, DPRED_E_ALIGN, DPRED_E_CUDA.
+ * Asynchronous on `stream`.
+ */
+#define DPRED_SCHED_RING 0
+#define DPRED_SCHED_BIDIR_RING 1
+#define DPRED_SCHED_RECURSIVE_DOUBLING 2
+int dpred_allgather_schedule_steps(int32_t schedule, int32_t n_nodes);
+int dpred_allgather_schedule_init(int32_t schedule, int32_t n_nodes, int64_t shard_elems, int32_t dtype,
+                                  const void* in, void* bufs, void* stream);
+int dpred_allgather_schedule_step(int32_t schedule, int32_t n_nodes, int64_t shard_elems, int32_t dtype, void* bufs,
+                                  int32_t step, void* stream);
+
+/*
  * Device error word: 0, or the DPRED_E_* code of the first device-side
  * failure (a bounded wait that gave up, an internal consistency check) since
  * the last clear.  Synchronises the current device.  clear != 0 resets it.

@@ -50,6 +50,7 @@ def lib():
         L.orc_allgather.argtypes = [i32, i64, i32, vp, vp, i32]
         L.orc_ring_allgather_steps.argtypes = [i32, vp, vp]
         L.orc_rd_allgather_steps.argtypes = [i32, vp, vp, vp, vp, vp]
+        L.orc_bidir_ring_allgather_steps.argtypes = [i32, vp, vp]
         _lib = L
     return _lib
 
@@ -286,6 +287,16 @@ def rd_steps(n: int) -> dict:
                                         final.ctypes.data, recv.ctypes.data), "recursive doubling steps")
     return {"partner": partner[:steps], "xfer_chunks": xfer[:steps], "held_chunks": held[:steps],
             "final": final, "recv_chunks": recv}
+
+
+def bidir_ring_steps(n: int) -> dict:
+    steps = n // 2
+    hold = np.empty((steps + 1, n, n), np.int32)
+    recv = np.empty(n, np.int64)
+    rc = lib().orc_bidir_ring_allgather_steps(n, hold.ctypes.data, recv.ctypes.data)
+    if rc < 0:
+        raise ValueError(f"bidirectional ring simulation failed ({rc})")
+    return {"steps": rc, "hold": hold, "recv_chunks": recv}
 
 
 # ----------------------------------------------------------- closed forms ---

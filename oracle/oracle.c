@@ -581,3 +581,39 @@ int orc_bucket_relayout(int world, int esize, const void* grads, int64_t ld, int
     free(first);
     return 0;
 }
+
+/* [AG] "Ring AllGather", the bidirectional ring (eq. ag-bidir-ring): data
+ * moves both ways round the ring at once, so ceil((N-1)/2) steps suffice.  In
+ * step s node i receives chunk (i - s) mod N from its left neighbour and chunk
+ * (i + s) mod N from its right neighbour (the same chunk once when they
+ * coincide).  Chunks are kept at their own index (canonical placement).
+ * hold is [steps + 1][N][N]: hold[s][i][c] = c when node i holds chunk c after
+ * step s, else -1.  recv[i] = chunks node i received.  Returns the number of
+ * steps, or -1. */
+int orc_bidir_ring_allgather_steps(int n, int32_t* hold, int64_t* recv) {
+    if (n < 1 || n > 64) return -1;
+    int steps = n / 2;            /* ceil((n - 1) / 2) */
+    uint64_t have[64];
+    for (int i = 0; i < n; ++i) {
+        have[i] = 1ull << i;
+        recv[i] = 0;
+    }
+    for (int i = 0; i < n; ++i)
+        for (int c = 0; c < n; ++c) hold[(0 * n + i) * n + c] = ((have[i] >> c) & 1ull) ? c : -1;
+    for (int s = 1; s <= steps; ++s) {
+        uint64_t next[64];
+        for (int i = 0; i < n; ++i) {
+            int from_left = ((i - s) % n + n) % n, from_right = (i + s) % n;
+            uint64_t add = (1ull << from_left) | (1ull << from_right);
+            /* the chunk from the left must be held by the left neighbour, the chunk from the right by the right one */
+            if (!((have[(i - 1 + n) % n] >> from_left) & 1ull) || !((have[(i + 1) % n] >> from_right) & 1ull)) return -2;
+            uint64_t fresh = add & ~have[i];
+            for (int c = 0; c < n; ++c) recv[i] += (fresh >> c) & 1ull;
+            next[i] = have[i] | add;
+        }
+        for (int i = 0; i < n; ++i) have[i] = next[i];
+        for (int i = 0; i < n; ++i)
+            for (int c = 0; c < n; ++c) hold[((int64_t)s * n + i) * n + c] = ((have[i] >> c) & 1ull) ? c : -1;
+    }
+    return steps;
+}

@@ -112,3 +112,25 @@ def test_allgather_is_a_pure_copy(order):
         for c in range(N):
             src = c if order == 0 else (i - c) % N
             assert np.array_equal(out[i, c * S:(c + 1) * S], x[src])
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 9, 16])
+def test_bidirectional_ring_steps_and_receive(N):
+    """eq. ag-bidir-ring: ceil((N-1)/2) steps; every node ends with all chunks
+    and receives (N-1)/N of M (eq. allgather-recv)."""
+    sim = oracle.bidir_ring_steps(N)
+    assert sim["steps"] == math.ceil((N - 1) / 2)
+    assert np.array_equal(sim["hold"][-1], np.tile(np.arange(N), (N, 1)))
+    assert np.all(sim["recv_chunks"] == N - 1)
+    # each step adds at most two chunks per node
+    for s in range(1, sim["steps"] + 1):
+        grown = (sim["hold"][s] >= 0).sum(axis=1) - (sim["hold"][s - 1] >= 0).sum(axis=1)
+        assert np.all((grown >= 1) & (grown <= 2))
+
+
+def test_bidirectional_ring_n4_by_hand():
+    sim = oracle.bidir_ring_steps(4)
+    held = lambda s, i: [int(c) for c in sim["hold"][s, i] if c >= 0]  # noqa: E731
+    assert held(1, 0) == [0, 1, 3]          # A gets B from the right and D from the left
+    assert held(2, 0) == [0, 1, 2, 3]       # C arrives from both sides at once
+    assert held(1, 2) == [1, 2, 3]

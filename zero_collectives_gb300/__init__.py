@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         L.dpred_bucket_relayout_workspace_bytes.argtypes = [i32, i32]
         L.dpred_bucket_relayout.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i64, i64, vp, i64, vp, vp,
                                             ctypes.c_size_t, vp]
+        L.dpred_allgather_schedule_steps.argtypes = [i32, i32]
+        L.dpred_allgather_schedule_init.argtypes = [i32, i32, i64, i32, vp, vp, vp]
+        L.dpred_allgather_schedule_step.argtypes = [i32, i32, i64, i32, vp, i32, vp]
         L.dpred_accumulator_save.argtypes = [i32, i64, vp, vp, vp]
         L.dpred_accumulator_restore.argtypes = [i32, i64, vp, vp, vp]
         L.dpred_reduce_scatter.argtypes = [i32, i64, i32, vp, i32, vp, i32, vp]
@@ -408,6 +411,32 @@ def set_flush_path(path: int) -> int:
 def selftest_wait_timeout(budget_cycles: int = 2_000_000, stream=None) -> None:
     """Launch a kernel whose bounded wait must give up (see dpred_selftest_wait_timeout)."""
     _check(lib().dpred_selftest_wait_timeout(int(budget_cycles), _stream(stream)))
+
+
+SCHED_RING, SCHED_BIDIR_RING, SCHED_RECURSIVE_DOUBLING = 0, 1, 2
+
+
+def allgather_schedule_steps(schedule: int, n_nodes: int) -> int:
+    rc = lib().dpred_allgather_schedule_steps(schedule, n_nodes)
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def allgather_schedule_init(schedule: int, inp, bufs, stream=None):
+    """inp: [N, S] shards; bufs: [N, N*S] node buffers (same dtype)."""
+    N, S = inp.shape
+    if tuple(bufs.shape) != (N, N * S) or bufs.dtype != inp.dtype or not bufs.is_contiguous() \
+            or not inp.is_contiguous():
+        raise ValueError("bufs must be contiguous [N, N*S] of the shards' dtype")
+    _check(lib().dpred_allgather_schedule_init(schedule, N, S, _dtype_code(inp), inp.data_ptr(), bufs.data_ptr(),
+                                               _stream(stream)))
+
+
+def allgather_schedule_step(schedule: int, bufs, step: int, stream=None):
+    N = bufs.shape[0]
+    _check(lib().dpred_allgather_schedule_step(schedule, N, bufs.shape[1] // N, _dtype_code(bufs), bufs.data_ptr(),
+                                               int(step), _stream(stream)))
 
 
 def device_status(clear: bool = False) -> int:
