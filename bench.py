@@ -543,8 +543,69 @@ def rows(peak):
         out[f"torch_zero_fill_{N}GiB"] = entry(ms, N * Mel * 2, workload="write-only reference (torch zero_)")
         del wr
         del ag, rs
+    out["allgather_schedules_N8"] = schedule_fit(8, Mel)
     torch.cuda.empty_cache()
     return out
+
+
+def schedule_fit(N, M):
+    """Ring, bidirectional ring and recursive doubling run step by step (one
+    copy launch per step) on N node buffers; per-step CUDA-event times fitted to
+    t = alpha + bytes / beta, and the page's closed forms (eqs. ring-ag,
+    ag-bidir-ring, rd-ag) evaluated with that alpha and the per-node
+    beta' = beta / (2N) (every step moves N chunks in and out of one HBM)."""
+    import numpy as np
+    import torch
+    import datagen
+    import zero_collectives_gb300 as zc
+    from datagen import BF16, UNIFORM
+    S = M // N
+    s = torch.cuda.current_stream()
+    x = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
+    datagen.fill_device(x.data_ptr(), N, S, S, BF16, UNIFORM, 5, 0, 1, 0, 1.0, s.cuda_stream)
+    bufs = torch.empty((N, N * S), dtype=torch.bfloat16, device="cuda")
+    cb = S * 2
+    pts, totals = [], {}
+    names = {zc.SCHED_RING: "ring", zc.SCHED_BIDIR_RING: "bidir_ring", zc.SCHED_RECURSIVE_DOUBLING: "recursive_doubling"}
+    for sched, name in names.items():
+        steps = zc.allgather_schedule_steps(sched, N)
+        best = None
+        for rep in range(4):
+            zc.allgather_schedule_init(sched, x, bufs)
+            ev = events(steps + 1)
+            ev[0].record(s)
+            for k in range(1, steps + 1):
+                zc.allgather_schedule_step(sched, bufs, k)
+                ev[k].record(s)
+            torch.cuda.synchronize()
+            t = [ev[k - 1].elapsed_time(ev[k]) for k in range(1, steps + 1)]
+            if rep and (best is None or sum(t) < sum(best)):
+                best = t
+        for k, tk in enumerate(best, start=1):
+            if sched == zc.SCHED_RING:
+                chunks = N
+            elif sched == zc.SCHED_BIDIR_RING:
+                chunks = N * (1 if (N % 2 == 0 and k == N // 2) else 2)
+            else:
+                chunks = N * (1 << (k - 1))
+            pts.append((2 * chunks * cb, tk * 1e-3))
+        totals[name] = {"steps": steps, "measured_ms": round(sum(best), 4), "step_ms": [round(v, 4) for v in best]}
+    b = np.array([p[0] for p in pts], dtype=np.float64)
+    t = np.array([p[1] for p in pts], dtype=np.float64)
+    A = np.stack([np.ones_like(b), b], axis=1)
+    (alpha, inv_beta), *_ = np.linalg.lstsq(A, t, rcond=None)
+    beta = 1.0 / inv_beta
+    beta_node = beta / (2 * N)
+    Mb = M * 2
+    from zero_collectives_gb300 import costs
+    model = {"ring": costs.ring(N, Mb, alpha, beta_node),
+             "bidir_ring": costs.bidirectional_ring(N, Mb, alpha, beta_node),
+             "recursive_doubling": costs.recursive_doubling(N, Mb, alpha, beta_node)}
+    for name in totals:
+        totals[name]["model_ms"] = round(model[name] * 1e3, 4)
+    del x, bufs
+    return {"alpha_us": round(alpha * 1e6, 2), "beta_GBps": round(beta / 1e9, 1),
+            "beta_per_node_GBps": round(beta_node / 1e9, 1), "M_bytes": Mb, "schedules": totals}
 
 
 # ------------------------------------------------------ reference (oracle) ---

@@ -134,3 +134,14 @@ def test_bidirectional_ring_n4_by_hand():
     assert held(1, 0) == [0, 1, 3]          # A gets B from the right and D from the left
     assert held(2, 0) == [0, 1, 2, 3]       # C arrives from both sides at once
     assert held(1, 2) == [1, 2, 3]
+
+
+@pytest.mark.parametrize("N", [2, 4, 8, 16])
+def test_product_cost_model_agrees_with_the_oracle_forms(N):
+    from zero_collectives_gb300 import costs
+    M, a, b = 1e9, 3e-6, 5e10
+    assert costs.ring(N, M, a, b) == pytest.approx(oracle.ring_ag_time(N, M, a, b))
+    assert costs.bidirectional_ring(N, M, a, b) == pytest.approx(oracle.bidir_ring_ag_time(N, M, a, b))
+    assert costs.recursive_doubling(N, M, a, b) == pytest.approx(oracle.rd_ag_time(N, M, a, b))
+    lat, bw = costs.lower_bounds(N, M, a, b)
+    assert lat == pytest.approx(oracle.ag_latency_lower_bound(N, a)) and bw == pytest.approx(oracle.ag_bw_lower_bound(N, M, 1, b))
