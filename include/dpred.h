@@ -120,6 +120,21 @@ int dpred_build_owner_map(int32_t world, int32_t rank, const dpred_group* groups
                           int32_t* n_owned, int32_t* n_total);
 
 /*
+ * The owner map of one parameter group, computed on the device (for an
+ * executor whose parameter table lives in device memory).  Same rule and
+ * results as dpred_build_owner_map for a single group: numel (device, int64
+ * [n_params]) in flat order; comm_ranks (device, int32 [comm_size]) or NULL
+ * for the identity; outputs owner / holder_lo / holder_hi (device, int32
+ * [n_params]) and counts (device, int32 [2]: n_owned, n_total).  One CTA:
+ * warp-shuffle reduction of the sizes for the partition size, warp-shuffle
+ * exclusive scan for the flat starts, warp ballots for the owned count.
+ * Errors: DPRED_E_INVAL, DPRED_E_ALIGN, DPRED_E_CUDA.  Asynchronous on `stream`.
+ */
+int dpred_build_owner_map_device(int32_t world, int32_t n_params, const int64_t* numel, int32_t comm_size,
+                                 const int32_t* comm_ranks, int32_t reduce_to_owner, int32_t* owner,
+                                 int32_t* holder_lo, int32_t* holder_hi, int32_t* counts, void* stream);
+
+/*
  * Probe counters of a flush from its metadata alone, without launching
  * anything ([DS] "reduce_probe": size the win before turning the path on).
  * Arguments as for dpred_flush_bucket.  kept_elems[r] sums the tasks whose

@@ -60,6 +60,7 @@ def lib() -> ctypes.CDLL:
         L.dpred_last_error.restype = ctypes.c_char_p
         L.dpred_version.restype = ctypes.c_char_p
         L.dpred_build_owner_map.argtypes = [i32, i32, vp, i32, i32, vp, vp, vp, vp, vp]
+        L.dpred_build_owner_map_device.argtypes = [i32, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp]
         L.dpred_flush_probe.argtypes = [i32, vp, i32, vp, i32, vp, i32, vp]
         L.dpred_flush_workspace_bytes.restype = ctypes.c_size_t
         L.dpred_flush_workspace_bytes.argtypes = [i32, i32]
@@ -154,6 +155,27 @@ def build_owner_map(world: int, groups, reduce_to_owner: bool = True, rank: int 
     _check(lib().dpred_build_owner_map(world, rank, arr, len(groups), int(reduce_to_owner), owner.ctypes.data,
                                        lo.ctypes.data, hi.ctypes.data, ctypes.byref(n_owned), ctypes.byref(n_total)))
     return OwnerMap(owner, lo, hi, n_owned.value, n_total.value)
+
+
+def build_owner_map_device(world: int, numel, comm_ranks=None, reduce_to_owner: bool = True, stream=None):
+    """Owner map of one group on the device.  numel: CUDA int64 tensor;
+    comm_ranks: CUDA int32 tensor or None.  Returns CUDA int32 tensors
+    (owner, holder_lo, holder_hi, counts[n_owned, n_total])."""
+    import torch
+    if numel.dtype != torch.int64 or not numel.is_cuda or not numel.is_contiguous():
+        raise ValueError("numel must be a contiguous CUDA int64 tensor")
+    n = numel.numel()
+    dev = numel.device
+    owner = torch.empty(n, dtype=torch.int32, device=dev)
+    lo = torch.empty(n, dtype=torch.int32, device=dev)
+    hi = torch.empty(n, dtype=torch.int32, device=dev)
+    counts = torch.empty(2, dtype=torch.int32, device=dev)
+    cs = world if comm_ranks is None else comm_ranks.numel()
+    _check(lib().dpred_build_owner_map_device(world, n, numel.data_ptr(), cs,
+                                              None if comm_ranks is None else comm_ranks.data_ptr(),
+                                              int(reduce_to_owner), owner.data_ptr(), lo.data_ptr(), hi.data_ptr(),
+                                              counts.data_ptr(), _stream(stream)))
+    return owner, lo, hi, counts
 
 
 # ------------------------------------------------------------------ probe ---
