@@ -321,10 +321,7 @@ def e2e(args, ex, grads, step_bytes, ws):
     stream = torch.cuda.current_stream()
 
     def step():
-        grads.copy_(host, non_blocking=True)
-        ex.flush_all(grads, probe=True)
-        for o, b in zip(outs, ex.grad.buf):
-            o.copy_(b, non_blocking=True)
+        ex.flush_all_from_host(host, outs, grads, probe=True)
 
     step()
     torch.cuda.synchronize()

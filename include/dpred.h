@@ -221,6 +221,49 @@ int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int
                                dpred_probe* probe, void* stream);
 
 /*
+ * The ZeRO-1 bucket-flush executor.  [DS] names Z1CustomOpExecutor::
+ * flushReduceBucket, which precomputes the roots of a whole bucket before
+ * issuing it and flushes each bucket when it is full.  An executor is bound
+ * to one gradient array (grads, device, [world, ld] of in_dtype) and to its
+ * buckets: bucket b covers columns [bucket_start[b], ...) with bucket_tasks[b]
+ * tasks, taken in order from the concatenated `tasks`, and its destination
+ * table of world * bucket_tasks[b] pointers, taken in order from the
+ * concatenated `dst` (same meaning as in dpred_flush_bucket; NULL = empty
+ * buffer).  dpred_executor_create validates every bucket with the flush's
+ * rules and prebuilds every launch plan and probe, so a flush is one kernel
+ * launch.  workspace (device) must hold the largest plan beyond the inline
+ * limit (dpred_flush_workspace_bytes) for as long as the executor is used.
+ * The executor keeps the flush counter of the probe lines.  Host memory only;
+ * no device memory is allocated.
+ *   dpred_executor_flush:     flush one bucket on `stream` (probe may be NULL).
+ *   dpred_executor_flush_all: flush every bucket in order (probes: NULL or
+ *                             one per bucket).
+ *   dpred_executor_flush_all_from_host: one step with host buffers.  The
+ *     bucket columns of host_grads ([world, host_ld], pinned host memory)
+ *     are copied into grads, each bucket is flushed, and everything each
+ *     bucket wrote is copied back into host memory: the destinations must lie
+ *     in the n_regions device regions region_dev[i] (region_bytes[i] bytes),
+ *     mirrored by pinned host regions region_host[i] at the same offsets.
+ *     The copies run on the executor's own streams, pipelined over buckets
+ *     (bucket b+1 arrives while bucket b is reduced; bucket b's results
+ *     leave as soon as it is done); `stream` waits for its earlier work first
+ *     and finishes after the last copy.  The first call creates the streams
+ *     and events.  Not re-entrant for one executor.
+ *   dpred_executor_destroy:   release the executor (after its work is done).
+ */
+typedef struct dpred_executor dpred_executor;
+int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div, int32_t reduce_to_owner,
+                          const int32_t* owner, int32_t n_params, const void* grads, int64_t ld, int32_t n_buckets,
+                          const int64_t* bucket_start, const int32_t* bucket_tasks, const dpred_task* tasks,
+                          void* const* dst, void* workspace, size_t workspace_bytes, dpred_executor** out);
+int dpred_executor_flush(dpred_executor* ex, int32_t bucket, dpred_probe* probe, void* stream);
+int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stream);
+int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
+                                       void* const* region_dev, void* const* region_host, const int64_t* region_bytes,
+                                       dpred_probe* probes, void* stream);
+int dpred_executor_destroy(dpred_executor* ex);
+
+/*
  * Partitioned flush: every rank receives exactly its optimizer partition's
  * slice of the reduced bucket.  [DS] "Describe alternatives you've considered"
  * (ncclReduceScatter over the bucket, "the better end state", same traffic

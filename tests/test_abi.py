@@ -220,3 +220,27 @@ def test_partitioned_and_relayout_validation(L):
     gap = np.array([0, 12], np.int64)
     assert L.dpred_bucket_relayout(2, 0, 0x10000, 100, tasks.ctypes.data, 2, gap.ctypes.data, 2, 30, 30, 0x40000, 60,
                                    used.ctypes.data, None, 0, None) == -1
+
+
+def test_executor_create_validates_and_destroys_without_a_gpu(L):
+    """Creating an executor only builds host plans: no device call happens."""
+    world = 4
+    tasks = _tasks([(0, 0, 64), (1, 64, 64)])
+    owner = np.array([0, -1], np.int32)
+    starts = np.array([0], np.int64)
+    counts = np.array([2], np.int32)
+    dst = (ctypes.c_void_p * (world * 2))(*[0x100000 + 4096 * i for i in range(world * 2)])
+    h = ctypes.c_void_p()
+    # owner task with buffers on non-owner ranks is fine unchecked; a bad owner value is not
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, 0x10000, 128, 1, starts.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == 0
+    assert h.value
+    assert L.dpred_executor_destroy(h) == 0
+    bad_owner = np.array([7, -1], np.int32)
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, bad_owner.ctypes.data, 2, 0x10000, 128, 1, starts.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == -1
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, 0x10000, 100, 1, starts.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == -3
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, 0x10000, 128, 1, starts.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, None, None, 0, ctypes.byref(h)) == -1
+    assert L.dpred_executor_flush(None, 0, None, None) == -1

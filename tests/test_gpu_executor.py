@@ -1,0 +1,77 @@
+"""The native executor: its flushes equal single dpred_flush_bucket calls bit
+for bit, the probe lines count flushes, and the host-buffer step (pipelined
+host-to-device copies, flushes, device-to-host copies) returns exactly what
+the device path computes."""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import zero_collectives_gb300 as zc
+from datagen import BF16, F32, NORMAL, workloads
+from tests.gpu_util import TORCH_DT, device_matrix
+
+pytestmark = pytest.mark.gpu
+
+
+def _setup(world, tree, capacity, dt=torch.bfloat16, seed=5):
+    layout = workloads.arrival_layout(tree, capacity=capacity)
+    code = BF16 if dt == torch.bfloat16 else F32
+    grads = device_matrix(world, tree.total, code, NORMAL, seed, sigma=1e-2)
+    ex = zc.Zero1Executor(world, tree.numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets], dt,
+                          fill=float("nan"))
+    return layout, grads, ex
+
+
+@pytest.mark.parametrize("world", [4, 8])
+def test_executor_equals_single_calls(world):
+    tree = workloads.straddle_tree(world, 40000 * world + 77, world - 1, pieces=5)
+    layout, grads, ex = _setup(world, tree, capacity=tree.total // 3)
+    assert len(layout.buckets) >= 3
+    lines = []
+    ex.probe_log = zc.ProbeLog(rank=0, sink=lines.append)
+    probes = ex.flush_all(grads, probe=True)
+    ref = zc.GradBuffers(world, ex.omap, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+    for i, b in enumerate(layout.buckets):
+        p = zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, ex.omap.owner, ref.dst_table(b.tasks), BF16,
+                            True, True, probe=True)
+        q = probes[i]
+        assert (p.tasks, p.reduced_elems, p.owner_elems, p.kept_elems) == \
+            (q.tasks, q.reduced_elems, q.owner_elems, q.kept_elems)
+    torch.cuda.synchronize()
+    for r in range(world):
+        assert torch.equal(ex.grad.buf[r].view(torch.int16), ref.buf[r].view(torch.int16))
+    assert [int(l.split("#")[1].split()[0]) for l in lines] == list(range(len(layout.buckets)))
+    ex.flush_all(grads)   # the counter keeps going
+    ex.close()
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
+def test_host_buffer_step_matches_device_path(dt):
+    world = 8
+    tree = workloads.straddle_tree(world, 300000 * world + 5, 5, pieces=4)
+    code = BF16 if dt == torch.bfloat16 else F32
+    layout, grads_dev, ex = _setup(world, tree, capacity=tree.total // 4, dt=dt)
+    ex.flush_all(grads_dev)
+    torch.cuda.synchronize()
+    want = [b.clone() for b in ex.grad.buf]
+    host = torch.empty((world, tree.total), dtype=dt, pin_memory=True)
+    arr = host.view(torch.int16 if dt == torch.bfloat16 else torch.int32).numpy()
+    datagen.fill_host(arr.view(np.uint16 if dt == torch.bfloat16 else np.float32), code, NORMAL, 5, sigma=1e-2)
+    outs = [torch.empty(b.shape, dtype=dt, pin_memory=True) for b in ex.grad.buf]
+    scratch = torch.zeros_like(grads_dev)
+    ex2 = zc.Zero1Executor(world, tree.numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets], dt,
+                           fill=float("nan"))
+    for _ in range(2):   # twice in a row: the pipeline's events and streams are reused
+        for o in outs:
+            o.fill_(float("nan"))
+        ex2.flush_all_from_host(host, outs, scratch)
+        torch.cuda.synchronize()
+        for r in range(world):
+            # everything a bucket wrote came back; the rest of the host buffer is untouched (NaN)
+            w = want[r].cpu()
+            written = ~torch.isnan(w.float())
+            assert torch.equal(outs[r][written].view(torch.int16 if dt == torch.bfloat16 else torch.int32),
+                               w[written].view(torch.int16 if dt == torch.bfloat16 else torch.int32))
+    ex.close()
+    ex2.close()

@@ -66,6 +66,12 @@ def lib() -> ctypes.CDLL:
         L.dpred_flush_workspace_bytes.argtypes = [i32, i32]
         L.dpred_flush_bucket.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp, vp,
                                          ctypes.c_size_t, vp]
+        L.dpred_executor_create.argtypes = [i32, i32, i32, i32, i32, vp, i32, vp, i64, i32, vp, vp, vp, vp, vp,
+                                            ctypes.c_size_t, vp]
+        L.dpred_executor_flush.argtypes = [vp, i32, vp, vp]
+        L.dpred_executor_flush_all.argtypes = [vp, vp, vp]
+        L.dpred_executor_flush_all_from_host.argtypes = [vp, vp, i64, i32, vp, vp, vp, vp, vp]
+        L.dpred_executor_destroy.argtypes = [vp]
         L.dpred_flush_bucket_noalloc.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp,
                                                  vp]
         L.dpred_accumulate_microbatch.argtypes = [i32, i64, vp, i32, vp, i32, i32, f32, vp, vp]
@@ -528,14 +534,16 @@ class GradBuffers:
 # ------------------------------------------------------- ZeRO-1 executor ---
 
 class Zero1Executor:
-    """Host runtime of the ZeRO-1 bucket flush on one GPU: the owner map, the
-    installed gradient buffers and one prebuilt destination table per bucket;
-    ``flush_all`` issues one dpred_flush_bucket per bucket on a stream (the
-    DeepSpeed issue's Z1CustomOpExecutor::flushReduceBucket, with the
-    collective replaced by the single-GPU kernel).
+    """The ZeRO-1 bucket-flush executor (dpred_executor_*): the owner map, the
+    installed gradient buffers and every bucket's prebuilt launch plan; a step
+    is one native call that flushes every bucket in order (the DeepSpeed
+    issue's Z1CustomOpExecutor::flushReduceBucket, with the collective replaced
+    by the single-GPU kernel).
 
     buckets: list of (start, tasks) -- the bucket's element offset in the
-    arrival-order gradient row and its TASK_DTYPE task table."""
+    arrival-order gradient row and its TASK_DTYPE task table.  The native
+    executor is bound to the gradient tensor of the first flush (and rebuilt
+    if a different tensor is passed)."""
 
     def __init__(self, world: int, numel, row_offset, buckets, dtype, reduce_to_owner: bool = True,
                  pre_div: bool = True, groups=None, probe_log: ProbeLog | None = None, fill=None):
@@ -553,18 +561,91 @@ class Zero1Executor:
         self.probe_log = probe_log
         ws = max((flush_workspace_bytes(world, len(t)) for _, t in self.buckets), default=0)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda") if ws else None
+        self._native = None
+        self._bound = None
+
+    def _bind(self, grads):
+        if grads.dim() != 2 or grads.stride(1) != 1 or grads.shape[0] != self.world:
+            raise ValueError("grads must be a [W, n] CUDA tensor with unit column stride")
+        ld = grads.stride(0) if self.world > 1 else grads.shape[1]
+        key = (grads.data_ptr(), ld, grads.dtype)
+        if self._bound == key:
+            return
+        self.close()
+        nb = len(self.buckets)
+        tasks = np.ascontiguousarray(np.concatenate([t for _, t in self.buckets]) if nb else np.zeros(0, TASK_DTYPE))
+        starts = np.array([s for s, _ in self.buckets], np.int64)
+        counts = np.array([len(t) for _, t in self.buckets], np.int32)
+        total = sum(self.world * len(t) for _, t in self.buckets)
+        dst = (ctypes.c_void_p * max(total, 1))()
+        pos = 0
+        for tab in self.tables:
+            n = tab.world * tab.n_tasks
+            for i in range(n):
+                dst[pos + i] = tab.c[i]
+            pos += n
+        handle = ctypes.c_void_p()
+        ws_ptr, ws_bytes = (None, 0) if self.workspace is None else (self.workspace.data_ptr(), self.workspace.numel())
+        _check(lib().dpred_executor_create(self.world, _dtype_code(grads), self.dt_code, int(self.pre_div),
+                                           int(self.reduce_to_owner), self.omap.owner.ctypes.data, len(self.omap.owner),
+                                           grads.data_ptr(), ld, nb, starts.ctypes.data, counts.ctypes.data,
+                                           tasks.ctypes.data, dst, ws_ptr, ws_bytes, ctypes.byref(handle)))
+        self._native = handle
+        self._bound = key
+
+    def close(self):
+        if self._native is not None and _lib is not None:
+            lib().dpred_executor_destroy(self._native)
+        self._native = None
+        self._bound = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _probes(self, want: bool):
+        return (_Probe * max(len(self.buckets), 1))() if want else None
+
+    def _finish(self, probes, probe: bool):
+        if probes is None:
+            return None
+        out = [_probe_from(probes[b], self.world) for b in range(len(self.buckets))]
+        if self.probe_log is not None:
+            for p in out:
+                self.probe_log.record(p, self.dt_code, self.pre_div)
+        return out if probe else None
 
     def flush_all(self, grads, stream=None, probe: bool = False):
-        """grads: CUDA tensor [W, n] (arrival-order rows).  Returns the probes when probe=True."""
-        probes = []
-        want = probe or self.probe_log is not None
-        for (start, tasks), size, table in zip(self.buckets, self.sizes, self.tables):
-            idx = self.probe_log.next_index() if self.probe_log is not None else len(probes)
-            p = flush_bucket(grads[:, start:start + size], tasks, self.omap.owner, table, self.dt_code,
-                             self.pre_div, self.reduce_to_owner, probe=want, flush_index=idx,
-                             workspace=self.workspace, stream=stream)
-            if self.probe_log is not None:
-                self.probe_log.record(p, self.dt_code, self.pre_div)
-            if probe:
-                probes.append(p)
-        return probes if probe else None
+        """Flush every bucket of grads ([W, n], arrival-order rows) on a stream.
+        Returns the probes when probe=True."""
+        self._bind(grads)
+        probes = self._probes(probe or self.probe_log is not None)
+        _check(lib().dpred_executor_flush_all(self._native, probes, _stream(stream)))
+        return self._finish(probes, probe)
+
+    def flush_bucket(self, grads, bucket: int, stream=None):
+        self._bind(grads)
+        _check(lib().dpred_executor_flush(self._native, int(bucket), None, _stream(stream)))
+
+    def flush_all_from_host(self, host_grads, host_bufs, grads, stream=None, probe: bool = False):
+        """One step with host buffers: host_grads (pinned [W, n]) is copied into
+        grads bucket by bucket, every bucket is flushed, and each rank's
+        gradient buffer is copied back into host_bufs[r] (pinned, same size),
+        pipelined over buckets on the executor's copy streams."""
+        self._bind(grads)
+        W = self.world
+        if len(host_bufs) != W:
+            raise ValueError("one host buffer per rank")
+        dev = (ctypes.c_void_p * W)(*[b.data_ptr() for b in self.grad.buf])
+        host = (ctypes.c_void_p * W)(*[h.data_ptr() for h in host_bufs])
+        nbytes = np.array([b.numel() * b.element_size() for b in self.grad.buf], np.int64)
+        for h, n in zip(host_bufs, nbytes):
+            if h.numel() * h.element_size() < n:
+                raise ValueError("host buffer smaller than its device buffer")
+        probes = self._probes(probe or self.probe_log is not None)
+        hld = host_grads.stride(0) if W > 1 else host_grads.shape[1]
+        _check(lib().dpred_executor_flush_all_from_host(self._native, host_grads.data_ptr(), hld, W, dev, host,
+                                                        nbytes.ctypes.data, probes, _stream(stream)))
+        return self._finish(probes, probe)

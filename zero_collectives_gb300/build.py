@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdpred.so")
 OBJDIR = os.path.join(HERE, "_build")
-SOURCES = ["abi.cu", "flush_bf16.cu", "flush_f32.cu", "accumulate.cu", "allgather.cu", "noalloc.cu", "selftest.cu", "relayout.cu", "schedule.cu", "owner_map.cu"]
+SOURCES = ["abi.cu", "flush_bf16.cu", "flush_f32.cu", "accumulate.cu", "allgather.cu", "noalloc.cu", "selftest.cu", "relayout.cu", "schedule.cu", "owner_map.cu", "executor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", *ARCH, "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC", "-I", INCLUDE,
               "-I", CSRC]

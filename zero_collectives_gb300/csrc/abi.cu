@@ -19,39 +19,23 @@ namespace {
 int g_flush_path = PATH_AUTO;
 }
 
-int flush_path() { return g_flush_path; }
-
-namespace {
-thread_local std::string t_last_error;
-
-int elem_size(int dt) { return dt == DPRED_BF16 ? 2 : 4; }
-bool dtype_ok(int dt) { return dt == DPRED_BF16 || dt == DPRED_F32; }
-bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
-bool pow2(int w) { return w > 0 && (w & (w - 1)) == 0; }
-
-struct Dest {
-    int64_t src_off, numel;
-    std::vector<void*> ptrs;  // delivered, non-empty destinations (element 0 of the task)
-};
-
-// Turn per-task destination lists into the kernel plan and launch it.  Tasks
-// with no destination write nothing and are left out of the plan.
-int run_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, int pre_div,
-             const std::vector<Dest>& tasks, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+// Tasks with no destination write nothing and are left out of the plan.
+void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, int pre_div,
+                const std::vector<Dest>& tasks, BuiltPlan& out) {
     const int vec_elems = in_dt == DPRED_BF16 ? 8 : 4;
-    const int isz = elem_size(in_dt), osz = elem_size(out_dt);
+    const int isz = in_dt == DPRED_BF16 ? 2 : 4, osz = out_dt == DPRED_BF16 ? 2 : 4;
     const size_t out_align = std::min<size_t>(16, (size_t)vec_elems * osz);
-    const bool rows_vec = aligned(grads, 16) && (ld * isz) % 16 == 0;
-    std::vector<TaskDesc> plan;
-    std::vector<void*> pool;
-    plan.reserve(tasks.size());
+    const bool rows_vec = reinterpret_cast<uintptr_t>(grads) % 16 == 0 && (ld * isz) % 16 == 0;
+    out.tasks.clear();
+    out.pool.clear();
+    out.tasks.reserve(tasks.size());
     int64_t units = 0;
     for (const Dest& d : tasks) {
         if (d.numel == 0 || d.ptrs.empty()) continue;
         TaskDesc t{};
         t.src_off = d.src_off;
         t.numel = d.numel;
-        t.dst_begin = (int32_t)pool.size();
+        t.dst_begin = (int32_t)out.pool.size();
         t.ndst = (int16_t)d.ptrs.size();
         int64_t head = (vec_elems - d.src_off % vec_elems) % vec_elems;
         if (head > d.numel) head = d.numel;
@@ -62,28 +46,53 @@ int run_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, in
         t.head = vec ? (uint8_t)head : 0;
         t.unit_begin = units;
         units += flush_task_units(t, vec_elems);
-        pool.insert(pool.end(), d.ptrs.begin(), d.ptrs.end());
-        plan.push_back(t);
+        out.pool.insert(out.pool.end(), d.ptrs.begin(), d.ptrs.end());
+        out.tasks.push_back(t);
     }
-    if (plan.empty()) return DPRED_OK;
+    out.h = FlushHeader{};
+    out.h.grads = grads;
+    out.h.ld = ld;
+    out.h.total_units = units;
+    out.h.world = world;
+    out.h.n_tasks = (int32_t)out.tasks.size();
+    out.h.pdiv = (pre_div && world > 1) ? (((world & (world - 1)) == 0) ? PDIV_POW2 : PDIV_DIV) : PDIV_NONE;
+    out.h.wf = (float)world;
+    out.h.inv_w = 1.0f / (float)world;
+    out.in_dt = in_dt;
+    out.out_dt = out_dt;
+}
+
+int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    if (p.tasks.empty()) return DPRED_OK;
     FlushLaunch L{};
-    L.h.grads = grads;
+    L.h = p.h;
     L.h.err = device_error_word();
-    L.h.ld = ld;
-    L.h.total_units = units;
-    L.h.world = world;
-    L.h.n_tasks = (int32_t)plan.size();
-    L.h.pdiv = (pre_div && world > 1) ? (pow2(world) ? PDIV_POW2 : PDIV_DIV) : PDIV_NONE;
-    L.h.wf = (float)world;
-    L.h.inv_w = 1.0f / (float)world;
-    L.in_dt = in_dt;
-    L.out_dt = out_dt;
-    L.tasks = plan.data();
-    L.dst = pool.data();
-    L.n_dst = (int)pool.size();
+    L.in_dt = p.in_dt;
+    L.out_dt = p.out_dt;
+    L.tasks = p.tasks.data();
+    L.dst = p.pool.data();
+    L.n_dst = (int)p.pool.size();
     L.workspace = workspace;
     L.workspace_bytes = workspace_bytes;
-    return in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
+    return p.in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
+}
+
+int flush_path() { return g_flush_path; }
+
+namespace {
+thread_local std::string t_last_error;
+
+int elem_size(int dt) { return dt == DPRED_BF16 ? 2 : 4; }
+bool dtype_ok(int dt) { return dt == DPRED_BF16 || dt == DPRED_F32; }
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+bool pow2(int w) { return w > 0 && (w & (w - 1)) == 0; }
+
+// Turn per-task destination lists into a kernel plan and launch it.
+int run_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, int pre_div,
+             const std::vector<Dest>& tasks, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    BuiltPlan p;
+    build_plan(world, in_dt, grads, ld, out_dt, pre_div, tasks, p);
+    return launch_plan(p, workspace, workspace_bytes, s);
 }
 
 }  // namespace

@@ -122,6 +122,23 @@ inline int64_t flush_task_units(const TaskDesc& t, int vec_elems) {
     return (t.numel + kUnitScalar - 1) / kUnitScalar;
 }
 
+// Host-side plan of one flush launch.
+struct Dest {
+    int64_t src_off, numel;
+    std::vector<void*> ptrs;  // delivered, non-empty destinations (element 0 of the task)
+};
+
+struct BuiltPlan {
+    FlushHeader h;
+    int in_dt, out_dt;
+    std::vector<TaskDesc> tasks;
+    std::vector<void*> pool;
+};
+
+void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, int pre_div,
+                const std::vector<Dest>& tasks, BuiltPlan& out);
+int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s);
+
 int launch_flush_bf16_in(const FlushLaunch& L, cudaStream_t s);
 int launch_flush_f32_in(const FlushLaunch& L, cudaStream_t s);
 

@@ -1,0 +1,267 @@
+// executor.cu -- the native ZeRO-1 bucket-flush executor.
+//
+// DeepSpeed issue #8700: DeepCompile's ZeRO-1 executor (Z1CustomOpExecutor)
+// holds the owner map ("roots is therefore precomputed for the whole bucket
+// before any collective is issued") and flushes each reduce bucket when it is
+// full, with a probe line per flush.  This executor does the same on one GPU:
+// at creation it validates everything and builds every bucket's launch plan
+// (owners, delivered non-empty destinations, vector alignment, work units) and
+// its probe counters; a flush is then one kernel launch with no per-call host
+// work beyond copying the prebuilt plan into the launch.
+//
+// flush_all_from_host adds the host side of a step: the gradients arrive in
+// pinned host memory and the reduced gradients go back to host memory.  The
+// executor pipelines it over buckets on its own copy streams -- bucket b+1's
+// host-to-device copy overlaps bucket b's flush, and each bucket's results
+// start their device-to-host copy as soon as its flush ends -- and joins the
+// caller's stream at the end.
+#include <algorithm>
+#include <climits>
+#include <cstdint>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+
+struct dpred_executor {
+    int world, in_dt, out_dt;
+    const char* grads;  // device [world, ld]
+    int64_t ld;
+    std::vector<int64_t> start, size;             // per bucket: column range of the gradient rows
+    std::vector<dpred::BuiltPlan> plans;          // per bucket
+    std::vector<dpred_probe> probes;              // per bucket (flush_index filled per call)
+    std::vector<std::vector<std::pair<char*, int64_t>>> written;  // per bucket: [device pointer, bytes] written
+    void* workspace;
+    size_t workspace_bytes;
+    int64_t flushes = 0;
+    // host pipeline resources, created on first use
+    bool pipeline = false;
+    cudaStream_t h2d[2] = {nullptr, nullptr}, d2h = nullptr;
+    std::vector<cudaEvent_t> ev_in, ev_out;
+    cudaEvent_t ev_start = nullptr, ev_done = nullptr;
+    std::mutex mu;
+};
+
+namespace {
+
+int esz(int dt) { return dt == DPRED_BF16 ? 2 : 4; }
+
+int setup_pipeline(dpred_executor* ex) {
+    if (ex->pipeline) return DPRED_OK;
+    cudaError_t e = cudaSuccess;
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&ex->h2d[i], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ex->d2h, cudaStreamNonBlocking);
+    const size_t nb = ex->plans.size();
+    ex->ev_in.assign(nb, nullptr);
+    ex->ev_out.assign(nb, nullptr);
+    for (size_t b = 0; b < nb && e == cudaSuccess; ++b) {
+        e = cudaEventCreateWithFlags(&ex->ev_in[b], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ex->ev_out[b], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ex->ev_start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ex->ev_done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return dpred::cuda_error(e, "executor stream/event creation");
+    ex->pipeline = true;
+    return DPRED_OK;
+}
+
+void release(dpred_executor* ex) {
+    for (auto& s : ex->h2d)
+        if (s) cudaStreamDestroy(s);
+    if (ex->d2h) cudaStreamDestroy(ex->d2h);
+    for (auto e : ex->ev_in)
+        if (e) cudaEventDestroy(e);
+    for (auto e : ex->ev_out)
+        if (e) cudaEventDestroy(e);
+    if (ex->ev_start) cudaEventDestroy(ex->ev_start);
+    if (ex->ev_done) cudaEventDestroy(ex->ev_done);
+}
+
+}  // namespace
+
+extern "C" {
+
+int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div, int32_t reduce_to_owner,
+                          const int32_t* owner, int32_t n_params, const void* grads, int64_t ld, int32_t n_buckets,
+                          const int64_t* bucket_start, const int32_t* bucket_tasks, const dpred_task* tasks,
+                          void* const* dst, void* workspace, size_t workspace_bytes, dpred_executor** out) {
+    using namespace dpred;
+    if (!out) return set_error(DPRED_E_INVAL, "null executor output");
+    *out = nullptr;
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (n_buckets < 0 || (n_buckets > 0 && (!bucket_start || !bucket_tasks)))
+        return set_error(DPRED_E_INVAL, "bad bucket list");
+    auto ex = new (std::nothrow) dpred_executor();
+    if (!ex) return set_error(DPRED_E_INVAL, "out of host memory");
+    ex->world = world;
+    ex->in_dt = in_dtype;
+    ex->out_dt = out_dtype;
+    ex->grads = static_cast<const char*>(grads);
+    ex->ld = ld;
+    ex->workspace = workspace;
+    ex->workspace_bytes = workspace_bytes;
+    int64_t t0 = 0, d0 = 0;
+    for (int b = 0; b < n_buckets; ++b) {
+        const int nt = bucket_tasks[b];
+        if (nt < 0) {
+            delete ex;
+            return set_error(DPRED_E_INVAL, "bucket %d: negative task count", b);
+        }
+        const dpred_task* bt = tasks + t0;
+        void* const* bd = dst ? dst + d0 : nullptr;
+        int64_t width = 0;
+        for (int t = 0; t < nt; ++t) width = std::max(width, bt[t].offset + bt[t].numel);
+        if (bucket_start[b] < 0 || bucket_start[b] + width > ld) {
+            delete ex;
+            return set_error(DPRED_E_SIZE, "bucket %d: columns [%lld, %lld) outside the row of %lld", b,
+                             (long long)bucket_start[b], (long long)(bucket_start[b] + width), (long long)ld);
+        }
+        // Full validation through the public probe path (same rules as a flush).
+        dpred_probe pr{};
+        int rc = dpred_flush_probe(world, bt, nt, owner, n_params, bd, reduce_to_owner, &pr);
+        if (rc == DPRED_OK && ((in_dtype != DPRED_BF16 && in_dtype != DPRED_F32) ||
+                               (out_dtype != DPRED_BF16 && out_dtype != DPRED_F32)))
+            rc = set_error(DPRED_E_INVAL, "bad dtype");
+        if (rc == DPRED_OK && dst == nullptr) rc = set_error(DPRED_E_INVAL, "the executor needs destination tables");
+        if (rc == DPRED_OK && width > 0 && grads == nullptr) rc = set_error(DPRED_E_INVAL, "null grads");
+        if (rc == DPRED_OK && grads && reinterpret_cast<uintptr_t>(grads) % esz(in_dtype))
+            rc = set_error(DPRED_E_ALIGN, "grads not aligned to its element size");
+        if (rc) {
+            delete ex;
+            return rc;
+        }
+        std::vector<Dest> plan(nt);
+        std::vector<std::pair<char*, int64_t>> wr;
+        for (int t = 0; t < nt; ++t) {
+            const int root = (reduce_to_owner && owner && owner[bt[t].param_id] >= 0) ? owner[bt[t].param_id] : -1;
+            plan[t].src_off = bt[t].offset;
+            plan[t].numel = bt[t].numel;
+            for (int r = 0; r < world; ++r) {
+                if (root >= 0 && r != root) continue;
+                void* p = bd[(int64_t)r * nt + t];
+                if (!p) continue;
+                if (reinterpret_cast<uintptr_t>(p) % esz(out_dtype)) {
+                    delete ex;
+                    return set_error(DPRED_E_ALIGN, "bucket %d: destination not aligned to its element size", b);
+                }
+                plan[t].ptrs.push_back(p);
+                if (bt[t].numel > 0) wr.emplace_back(static_cast<char*>(p), bt[t].numel * esz(out_dtype));
+            }
+        }
+        BuiltPlan bp;
+        build_plan(world, in_dtype, static_cast<const char*>(grads) + bucket_start[b] * esz(in_dtype), ld, out_dtype,
+                   pre_div, plan, bp);
+        if (bp.h.n_tasks > kInlineTasks || (int)bp.pool.size() > kInlineDst) {
+            const size_t need = sizeof(TaskDesc) * bp.tasks.size() + ((bp.pool.size() * sizeof(void*) + 15) & ~(size_t)15);
+            if (!workspace || workspace_bytes < need) {
+                delete ex;
+                return set_error(DPRED_E_SIZE, "bucket %d needs %zu bytes of workspace, got %zu", b, need,
+                                 workspace_bytes);
+            }
+        }
+        ex->start.push_back(bucket_start[b]);
+        ex->size.push_back(width);
+        ex->plans.push_back(std::move(bp));
+        ex->probes.push_back(pr);
+        ex->written.push_back(std::move(wr));
+        t0 += nt;
+        d0 += (int64_t)world * nt;
+    }
+    *out = ex;
+    return DPRED_OK;
+}
+
+int dpred_executor_destroy(dpred_executor* ex) {
+    if (!ex) return DPRED_OK;
+    release(ex);
+    delete ex;
+    return DPRED_OK;
+}
+
+int dpred_executor_flush(dpred_executor* ex, int32_t bucket, dpred_probe* probe, void* stream) {
+    using namespace dpred;
+    if (!ex) return set_error(DPRED_E_INVAL, "null executor");
+    if (bucket < 0 || bucket >= (int)ex->plans.size())
+        return set_error(DPRED_E_INVAL, "bucket %d outside 0..%d", bucket, (int)ex->plans.size() - 1);
+    if (probe) {
+        *probe = ex->probes[bucket];
+        probe->flush_index = ex->flushes;
+    }
+    ex->flushes += 1;
+    return launch_plan(ex->plans[bucket], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stream) {
+    if (!ex) return dpred::set_error(DPRED_E_INVAL, "null executor");
+    for (int b = 0; b < (int)ex->plans.size(); ++b) {
+        int rc = dpred_executor_flush(ex, b, probes ? probes + b : nullptr, stream);
+        if (rc) return rc;
+    }
+    return DPRED_OK;
+}
+
+int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
+                                       void* const* region_dev, void* const* region_host, const int64_t* region_bytes,
+                                       dpred_probe* probes, void* stream) {
+    using namespace dpred;
+    if (!ex) return set_error(DPRED_E_INVAL, "null executor");
+    if (!host_grads || host_ld < 0) return set_error(DPRED_E_INVAL, "bad host gradients");
+    if (n_regions < 0 || (n_regions > 0 && (!region_dev || !region_host || !region_bytes)))
+        return set_error(DPRED_E_INVAL, "bad output regions");
+    const int isz = esz(ex->in_dt);
+    // every written destination range must lie inside one output region
+    std::vector<std::vector<std::pair<int, std::pair<int64_t, int64_t>>>> copies(ex->plans.size());
+    for (size_t b = 0; b < ex->plans.size(); ++b) {
+        std::vector<std::pair<int64_t, int64_t>> span(n_regions, {INT64_MAX, -1});
+        for (auto& w : ex->written[b]) {
+            int hit = -1;
+            for (int i = 0; i < n_regions && hit < 0; ++i) {
+                const char* base = static_cast<const char*>(region_dev[i]);
+                if (w.first >= base && w.first + w.second <= base + region_bytes[i]) hit = i;
+            }
+            if (hit < 0) return set_error(DPRED_E_INVAL, "bucket %zu writes outside every output region", b);
+            const int64_t off = w.first - static_cast<const char*>(region_dev[hit]);
+            span[hit].first = std::min(span[hit].first, off);
+            span[hit].second = std::max(span[hit].second, off + w.second);
+        }
+        for (int i = 0; i < n_regions; ++i)
+            if (span[i].second > span[i].first) copies[b].push_back({i, span[i]});
+    }
+    std::lock_guard<std::mutex> lock(ex->mu);
+    int rc = setup_pipeline(ex);
+    if (rc) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaEventRecord(ex->ev_start, s);  // earlier work on the caller's stream comes first
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(ex->h2d[i], ex->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ex->d2h, ex->ev_start, 0);
+    for (size_t b = 0; b < ex->plans.size() && e == cudaSuccess; ++b) {
+        // one contiguous copy per replica row: a pitched 2-D copy of a bucket
+        // moves several times slower over the host link on this platform
+        cudaStream_t cs = ex->h2d[0];
+        const int64_t col = ex->start[b] * isz;
+        for (int r = 0; r < ex->world && e == cudaSuccess; ++r)
+            e = cudaMemcpyAsync(const_cast<char*>(ex->grads) + r * ex->ld * isz + col,
+                                static_cast<const char*>(host_grads) + r * host_ld * isz + col,
+                                (size_t)(ex->size[b] * isz), cudaMemcpyHostToDevice, cs);
+        if (e == cudaSuccess) e = cudaEventRecord(ex->ev_in[b], cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ex->ev_in[b], 0);
+        if (e != cudaSuccess) break;
+        rc = dpred_executor_flush(ex, (int)b, probes ? probes + b : nullptr, stream);
+        if (rc) return rc;
+        e = cudaEventRecord(ex->ev_out[b], s);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(ex->d2h, ex->ev_out[b], 0);
+        for (auto& c : copies[b]) {
+            if (e != cudaSuccess) break;
+            const int i = c.first;
+            e = cudaMemcpyAsync(static_cast<char*>(region_host[i]) + c.second.first,
+                                static_cast<const char*>(region_dev[i]) + c.second.first,
+                                (size_t)(c.second.second - c.second.first), cudaMemcpyDeviceToHost, ex->d2h);
+        }
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(ex->ev_done, ex->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ex->ev_done, 0);  // the caller's stream completes last
+    return e == cudaSuccess ? DPRED_OK : cuda_error(e, "executor host pipeline");
+}
+
+}  // extern "C"
