@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--flush-path", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel family of the flush (results are bit-identical)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="flush sweep: bucket sizes 1 KB-1 GB per replica, W in {2,4,8,16}, bf16/fp32, eager and "
+                         "CUDA-graph replay; one JSON line per case")
     ap.add_argument("--row", choices=["allgather", "reduce_scatter", "accumulate"], default=None,
                     help="time one other hot-path row alone (small profiling cases) and print its JSON line")
     ap.add_argument("--row-nodes", type=int, default=8)
@@ -720,9 +723,78 @@ def single_row(args):
                       "frac_of_peak": round(gbs / peak, 4), "bytes": nbytes}), flush=True)
 
 
+def sweep(args):
+    """Config 5: one bucket of W-1 straddlers plus an excluded 3-parameter
+    group, bucket bytes per replica 1 KB .. 1 GB (x16), W in {2, 4, 8, 16},
+    bf16 and fp32, reduce-to-owner.  Eager executor flushes and the same step
+    replayed from a CUDA graph; inputs above ~2x L2 need no flush between
+    launches, smaller ones rotate over enough copies to exceed it."""
+    import numpy as np
+    import torch
+    import datagen
+    import zero_collectives_gb300 as zc
+    from datagen import BF16, F32, NORMAL, workloads
+    torch.cuda.set_device(0)
+    peak, _ = peaks()
+    s = torch.cuda.current_stream()
+    l2 = 129 * 2**20
+    for W in (2, 4, 8, 16):
+        for dt, code in ((torch.bfloat16, BF16), (torch.float32, F32)):
+            esize = 2 if code == BF16 else 4
+            for kb in (1, 16, 256, 4096, 65536, 1048576):
+                elems = max(kb * 1024 // esize, 64 * W)
+                tree = workloads.straddle_tree(W, elems, W - 1, pieces=2)
+                ex_sizes = np.array([96, 64, 32], np.int64)
+                numel = np.concatenate([tree.numel, ex_sizes])
+                groups = [(None, tree.numel), (list(range(max(1, W // 2))), ex_sizes)]
+                full = workloads.Tree([f"p{i}" for i in range(len(numel))], numel)
+                layout = workloads.arrival_layout(full, capacity=None)
+                copies = max(1, -(-2 * l2 // (W * full.total * esize)))
+                gs = []
+                for c in range(copies):
+                    g = torch.empty((W, full.total), dtype=dt, device="cuda")
+                    datagen.fill_device(g.data_ptr(), W, full.total, full.total, code, NORMAL, 6 + c, 0, 1, 0, 1e-3,
+                                        s.cuda_stream)
+                    gs.append(g)
+                exs = [zc.Zero1Executor(W, numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets], dt,
+                                        groups=groups) for _ in range(copies)]
+                for e, g in zip(exs, gs):
+                    e.flush_all(g)
+                nbytes = W * full.total * esize + sum(
+                    int(full.numel[p]) * esize * (1 if exs[0].omap.owner[p] >= 0 else
+                                                  int(exs[0].omap.holder_hi[p] - exs[0].omap.holder_lo[p]) + 1)
+                    for p in range(full.n_params))
+                reps = int(min(2000, max(20, 0.05 / max(nbytes / (peak * 1e9), 1e-6))))
+                reps = max(copies, reps - reps % copies)
+
+                def eager():
+                    for e, g in zip(exs, gs):
+                        e.flush_all(g)
+
+                ms_e = timed(eager, reps // copies, warm=3) / copies
+                side = torch.cuda.Stream()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=side):
+                    eager()
+                ms_g = timed(graph.replay, reps // copies, warm=3) / copies
+                line = {"sweep": True, "world": W, "dtype": "bf16" if code == BF16 else "f32",
+                        "bucket_bytes_per_replica": full.total * esize, "elems": full.total, "copies": copies,
+                        "bytes": nbytes, "eager_us": round(ms_e * 1e3, 2), "graph_us": round(ms_g * 1e3, 2),
+                        "eager_GBps": round(nbytes / (ms_e * 1e-3) / 1e9, 1),
+                        "graph_GBps": round(nbytes / (ms_g * 1e-3) / 1e9, 1),
+                        "graph_frac_of_peak": round(nbytes / (ms_g * 1e-3) / 1e9 / peak, 4)}
+                print(json.dumps(line), flush=True)
+                for e in exs:
+                    e.close()
+                del gs, exs, graph
+                torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
-    if args.row is not None:
+    if args.sweep:
+        sweep(args)
+    elif args.row is not None:
         single_row(args)
     elif args.impl == "reference":
         run_reference(args)

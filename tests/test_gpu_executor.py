@@ -75,3 +75,37 @@ def test_host_buffer_step_matches_device_path(dt):
                                w[written].view(torch.int16 if dt == torch.bfloat16 else torch.int32))
     ex.close()
     ex2.close()
+
+
+def test_step_captured_in_a_cuda_graph():
+    """A step whose plans travel inside the launches can be captured once and
+    replayed: replays give the eager result bit for bit, and follow new data
+    written into the same gradient tensor."""
+    world = 8
+    tree = workloads.straddle_tree(world, 20000 * world + 3, 4, pieces=3)
+    layout, grads, ex = _setup(world, tree, capacity=tree.total // 2)
+    ex.flush_all(grads)                      # eager: also does the one-time launch set-up
+    torch.cuda.synchronize()
+    eager = [b.clone() for b in ex.grad.buf]
+    for b in ex.grad.buf:
+        b.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        ex.flush_all(grads)
+    graph.replay()
+    torch.cuda.synchronize()
+    for r in range(world):
+        assert torch.equal(ex.grad.buf[r].view(torch.int16), eager[r].view(torch.int16))
+    # new gradients in the same tensor: the replay reduces them
+    datagen.fill_device(grads.data_ptr(), world, tree.total, tree.total, BF16, NORMAL, 99, 0, 1, 0, 1e-2,
+                        torch.cuda.current_stream().cuda_stream)
+    graph.replay()
+    fresh = zc.GradBuffers(world, ex.omap, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+    for b in layout.buckets:
+        zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, ex.omap.owner, fresh.dst_table(b.tasks), BF16,
+                        True, True)
+    torch.cuda.synchronize()
+    for r in range(world):
+        assert torch.equal(ex.grad.buf[r].view(torch.int16), fresh.buf[r].view(torch.int16))
+    ex.close()

@@ -37,7 +37,7 @@ struct dpred_executor {
     int64_t flushes = 0;
     // host pipeline resources, created on first use
     bool pipeline = false;
-    cudaStream_t h2d[2] = {nullptr, nullptr}, d2h = nullptr;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
     std::vector<cudaEvent_t> ev_in, ev_out;
     cudaEvent_t ev_start = nullptr, ev_done = nullptr;
     std::mutex mu;
@@ -50,7 +50,7 @@ int esz(int dt) { return dt == DPRED_BF16 ? 2 : 4; }
 int setup_pipeline(dpred_executor* ex) {
     if (ex->pipeline) return DPRED_OK;
     cudaError_t e = cudaSuccess;
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamCreateWithFlags(&ex->h2d[i], cudaStreamNonBlocking);
+    e = cudaStreamCreateWithFlags(&ex->h2d, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&ex->d2h, cudaStreamNonBlocking);
     const size_t nb = ex->plans.size();
     ex->ev_in.assign(nb, nullptr);
@@ -67,8 +67,7 @@ int setup_pipeline(dpred_executor* ex) {
 }
 
 void release(dpred_executor* ex) {
-    for (auto& s : ex->h2d)
-        if (s) cudaStreamDestroy(s);
+    if (ex->h2d) cudaStreamDestroy(ex->h2d);
     if (ex->d2h) cudaStreamDestroy(ex->d2h);
     for (auto e : ex->ev_in)
         if (e) cudaEventDestroy(e);
@@ -233,12 +232,12 @@ int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grad
     if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaEventRecord(ex->ev_start, s);  // earlier work on the caller's stream comes first
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(ex->h2d[i], ex->ev_start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ex->h2d, ex->ev_start, 0);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ex->d2h, ex->ev_start, 0);
     for (size_t b = 0; b < ex->plans.size() && e == cudaSuccess; ++b) {
         // one contiguous copy per replica row: a pitched 2-D copy of a bucket
         // moves several times slower over the host link on this platform
-        cudaStream_t cs = ex->h2d[0];
+        cudaStream_t cs = ex->h2d;
         const int64_t col = ex->start[b] * isz;
         for (int r = 0; r < ex->world && e == cudaSuccess; ++r)
             e = cudaMemcpyAsync(const_cast<char*>(ex->grads) + r * ex->ld * isz + col,
