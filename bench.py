@@ -45,7 +45,7 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the other hot-path rows")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--flush-path", choices=["auto", "ldg", "tma"], default="auto",
                     help="kernel family of the flush (results are bit-identical)")
@@ -328,6 +328,13 @@ def e2e(args, ex, grads, step_bytes, ws):
 
     step()
     torch.cuda.synchronize()
+    # the host link's own bandwidth in this run, for context: one plain copy
+    c0, c1 = events(2)
+    c0.record(stream)
+    grads.copy_(host, non_blocking=True)
+    c1.record(stream)
+    torch.cuda.synchronize()
+    link_gbs = host.numel() * host.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9
     barrier(ws)
     a, b = events(2)
     a.record(stream)
@@ -340,7 +347,8 @@ def e2e(args, ex, grads, step_bytes, ws):
     d2h = sum(o.numel() * o.element_size() for o in outs)
     return {"value": round(ws * step_bytes * args.e2e_steps / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "ms_per_step": round(ms / args.e2e_steps, 3)}
+            "ms_per_step": round(ms / args.e2e_steps, 3), "host_link_h2d_GBps": round(link_gbs, 1),
+            "path": "Zero1Executor.flush_all_from_host (dpred_executor_flush_all_from_host)"}
 
 
 def _cpu_flush_sample(buckets, tree, seconds):

@@ -30,6 +30,7 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     out.pool.clear();
     out.tasks.reserve(tasks.size());
     int64_t units = 0;
+    const int unit_vec = kUnitVec * flush_batch(world);
     for (const Dest& d : tasks) {
         if (d.numel == 0 || d.ptrs.empty()) continue;
         TaskDesc t{};
@@ -45,7 +46,7 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
         t.vec = vec ? 1 : 0;
         t.head = vec ? (uint8_t)head : 0;
         t.unit_begin = units;
-        units += flush_task_units(t, vec_elems);
+        units += flush_task_units(t, vec_elems, unit_vec);
         out.pool.insert(out.pool.end(), d.ptrs.begin(), d.ptrs.end());
         out.tasks.push_back(t);
     }
@@ -58,6 +59,7 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     out.h.pdiv = (pre_div && world > 1) ? (((world & (world - 1)) == 0) ? PDIV_POW2 : PDIV_DIV) : PDIV_NONE;
     out.h.wf = (float)world;
     out.h.inv_w = 1.0f / (float)world;
+    out.h.unit_vec = unit_vec;
     out.in_dt = in_dt;
     out.out_dt = out_dt;
 }

@@ -78,6 +78,7 @@ struct FlushHeader {
     int32_t n_tasks;
     int32_t pdiv;        // PreDiv
     float wf, inv_w;     // world as float, its reciprocal (exact for powers of two)
+    int32_t unit_vec;    // 16-byte vectors per work unit of the vector path
 };
 
 constexpr int kInlineTasks = 128;
@@ -99,7 +100,7 @@ struct FlushArgsWs {
 };
 
 constexpr int kFlushThreads = 256;
-constexpr int kUnitVec = 256;      // 16-byte vectors per work unit of the vector path (4 KB per row)
+constexpr int kUnitVec = 256;      // 16-byte vectors per thread-block pass of the vector path (4 KB per row)
 constexpr int kUnitScalar = 2048;  // elements per work unit of the scalar path
 
 struct FlushLaunch {
@@ -112,11 +113,16 @@ struct FlushLaunch {
     size_t workspace_bytes;
 };
 
-// Work units of a plan task; vec_elems = input elements per 16-byte vector.
-inline int64_t flush_task_units(const TaskDesc& t, int vec_elems) {
+// Vectors each thread keeps in flight per replica row: small world sizes take
+// several so that every SM still has enough bytes outstanding.
+inline int flush_batch(int world) { return world == 2 ? 4 : (world == 4 ? 2 : 1); }
+
+// Work units of a plan task; vec_elems = input elements per 16-byte vector,
+// unit_vec = vectors per unit (kUnitVec x the batch).
+inline int64_t flush_task_units(const TaskDesc& t, int vec_elems, int unit_vec) {
     if (t.vec) {
         int64_t nbody = (t.numel - t.head) / vec_elems;
-        int64_t u = (nbody + kUnitVec - 1) / kUnitVec;
+        int64_t u = (nbody + unit_vec - 1) / unit_vec;
         return u > 0 ? u : 1;
     }
     return (t.numel + kUnitScalar - 1) / kUnitScalar;

@@ -40,6 +40,9 @@ struct Elem<float> {
     __device__ static void store(float* p, float v) { *p = v; }
 };
 
+template <typename Args>
+__device__ __forceinline__ int64_t h_unit(const Args& a) { return a.h.unit_vec; }
+
 __device__ __forceinline__ const TaskDesc& plan_task(const FlushArgsInline& a, int i) { return a.tasks[i]; }
 __device__ __forceinline__ const TaskDesc& plan_task(const FlushArgsWs& a, int i) { return a.tasks[i]; }
 __device__ __forceinline__ void* plan_dst(const FlushArgsInline& a, int i) { return a.dst[i]; }
@@ -118,34 +121,37 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
     const FlushHeader& h = a.h;
     const int64_t stride = h.ld / VEC;  // row stride in vectors
     const uint4* base = reinterpret_cast<const uint4*>(static_cast<const Tin*>(h.grads) + T.src_off + T.head);
+#pragma unroll 1
     for (int64_t vb = v0 + threadIdx.x; vb < v1; vb += (int64_t)kFlushThreads * BATCH) {
         float y[BATCH][VEC];
         if constexpr (W_T > 0) {
+            // Out-of-range vectors of the last pass re-read vector vb (always
+            // in range) instead of branching, and are not stored.
             uint4 q[W_T][BATCH];
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
-                int64_t v = vb + (int64_t)b * kFlushThreads;
-                if (v < v1) {
+                const int64_t v = vb + (int64_t)b * kFlushThreads < v1 ? vb + (int64_t)b * kFlushThreads : vb;
 #pragma unroll
-                    for (int r = 0; r < W_T; ++r) q[r][b] = __ldcs(base + r * stride + v);
-                }
+                for (int r = 0; r < W_T; ++r) q[r][b] = __ldcs(base + r * stride + v);
             }
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
-                if (vb + (int64_t)b * kFlushThreads < v1) {
 #pragma unroll
-                    for (int r = 0; r < W_T; ++r) fold<Tin, MODE>(y[b], q[r][b], r == 0, h.wf, h.inv_w);
-                }
+                for (int r = 0; r < W_T; ++r) fold<Tin, MODE>(y[b], q[r][b], r == 0, h.wf, h.inv_w);
             }
         } else {
             // Any world size: rows in chunks of 8 loads in flight, folded in rank order.
             static_assert(BATCH == 1, "generic path keeps one vector per thread");
             int64_t v = vb;
             for (int r0 = 0; r0 < h.world; r0 += 8) {
+                // rows past the last one re-read the last row (no branch around
+                // the loads) and are not folded
                 uint4 q[8];
 #pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (r0 + r < h.world) q[r] = __ldcs(base + (int64_t)(r0 + r) * stride + v);
+                for (int r = 0; r < 8; ++r) {
+                    const int row = r0 + r < h.world ? r0 + r : h.world - 1;
+                    q[r] = __ldcs(base + (int64_t)row * stride + v);
+                }
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
                     if (r0 + r < h.world) fold<Tin, MODE>(y[0], q[r], r0 + r == 0, h.wf, h.inv_w);
@@ -168,8 +174,8 @@ __device__ __forceinline__ void flush_unit(const Args& a, const TaskDesc& T, int
     constexpr int VEC = Elem<Tin>::kVec;
     if (T.vec) {
         const int64_t nbody = (T.numel - T.head) / VEC;
-        const int64_t v0 = local * kUnitVec;
-        const int64_t v1 = v0 + kUnitVec < nbody ? v0 + kUnitVec : nbody;
+        const int64_t v0 = local * h_unit(a);
+        const int64_t v1 = v0 + h_unit(a) < nbody ? v0 + h_unit(a) : nbody;
         flush_unit_vec<W_T, BATCH, Tin, Tout, MODE>(a, T, v0, v1);
         if (local == 0) {
             const int tail = (int)(T.numel - T.head - nbody * VEC);
@@ -267,8 +273,8 @@ __device__ void tma_consume(const Args& a, unsigned char* smem, uint64_t* full, 
             continue;
         }
         const int64_t nbody = (T.numel - T.head) / VEC;
-        const int64_t v0 = local * kUnitVec;
-        const int64_t v1 = v0 + kUnitVec < nbody ? v0 + kUnitVec : nbody;
+        const int64_t v0 = local * (int64_t)h.unit_vec;
+        const int64_t v1 = v0 + h.unit_vec < nbody ? v0 + h.unit_vec : nbody;
         if (local == 0) {
             const int tail = (int)(T.numel - T.head - nbody * VEC);
             if (ctid < T.head)
@@ -319,8 +325,8 @@ __device__ void tma_produce(const Args& a, unsigned char* smem, uint64_t* full, 
         if (!T.vec) continue;
         const int64_t local = u - T.unit_begin;
         const int64_t nbody = (T.numel - T.head) / VEC;
-        const int64_t v0 = local * kUnitVec;
-        const int64_t v1 = v0 + kUnitVec < nbody ? v0 + kUnitVec : nbody;
+        const int64_t v0 = local * (int64_t)h.unit_vec;
+        const int64_t v1 = v0 + h.unit_vec < nbody ? v0 + h.unit_vec : nbody;
         const char* base = reinterpret_cast<const char*>(static_cast<const Tin*>(h.grads) + T.src_off + T.head);
         const int64_t row_bytes = h.ld * (int64_t)sizeof(Tin);
         for (int64_t sv = v0; sv < v1; sv += kSubVec) {
@@ -452,8 +458,8 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
 template <typename Tin, typename Tout>
 int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
     switch (L.h.world) {
-        case 2: return launch_flush_w<2, 1, Tin, Tout>(L, s);
-        case 4: return launch_flush_w<4, 1, Tin, Tout>(L, s);
+        case 2: return launch_flush_w<2, 4, Tin, Tout>(L, s);  // batch = flush_batch(world)
+        case 4: return launch_flush_w<4, 2, Tin, Tout>(L, s);
         case 8: return launch_flush_w<8, 1, Tin, Tout>(L, s);
         case 16: return launch_flush_w<16, 1, Tin, Tout>(L, s);
         default: return launch_flush_w<0, 1, Tin, Tout>(L, s);
