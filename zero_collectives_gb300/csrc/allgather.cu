@@ -136,13 +136,9 @@ int launch_allgather(int n_nodes, int64_t shard_elems, int esize, const void* in
                      (shard_bytes % 16 == 0);
     if (v16 && flush_path() != PATH_LDG) {  // auto: the TMA form measured faster on GB300
         constexpr size_t smem = (size_t)kAgStages * kAgTile;
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(allgather_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)smem);
-            if (e != cudaSuccess) return cuda_error(e, "allgather shared-memory attribute");
-            attr = true;
-        }
+        static bool attr[64] = {};
+        cudaError_t ea = ensure_smem_attr(allgather_tma_kernel, (int)smem, attr);
+        if (ea != cudaSuccess) return cuda_error(ea, "allgather shared-memory attribute");
         const int64_t tiles = ((shard_bytes + kAgTile - 1) / kAgTile) * n_nodes;
         const int64_t g = tiles < sm_count() ? tiles : sm_count();
         allgather_tma_kernel<<<(unsigned)g, 32, smem, s>>>(static_cast<const char*>(in), static_cast<char*>(out),

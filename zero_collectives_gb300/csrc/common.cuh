@@ -27,6 +27,22 @@ int cuda_error(cudaError_t e, const char* what);
 
 int sm_count();  // SMs of the current device (cached per device)
 
+// Apply a kernel's dynamic shared-memory limit once per device; `done` is that
+// kernel's per-device flag array (the attribute is per device context).
+template <typename K>
+cudaError_t ensure_smem_attr(K kernel, int bytes, bool (&done)[64]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (e != cudaSuccess) return e;
+        done[dev] = true;
+    }
+    return cudaSuccess;
+}
+
 // ---------------------------------------------------------- element math ---
 
 // Pre-division modes: none, multiply by the exact reciprocal of a power-of-two

@@ -407,12 +407,9 @@ cudaError_t launch_kernel(const Args& a, int64_t units, cudaStream_t s) {
         if (flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
             auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
             constexpr size_t smem = tma_smem_bytes<W_T>();
-            static bool attr = false;
-            if (!attr) {
-                cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-                if (e != cudaSuccess) return e;
-                attr = true;
-            }
+            static bool attr[64] = {};
+            cudaError_t ea = ensure_smem_attr(k, (int)smem, attr);
+            if (ea != cudaSuccess) return ea;
             int64_t g = sm_count();
             k<<<(unsigned)(units < g ? units : g), kTmaThreads, smem, s>>>(a);
             return cudaGetLastError();
