@@ -278,7 +278,8 @@ def run_dpred(args):
     result = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded Irwin-Hall normal, sigma 1e-3)",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic (seeded Irwin-Hall normal, sigma 1e-3)",
         "config": {"workload": WORKLOAD, "world": WORLD, "params": tree.n_params, "elems_per_replica": step_elems,
                    "buckets": len(buckets), "bucket_capacity": 52_428_800, "reduce_to_owner": True, "pre_div": True,
                    "parallelism": f"{ws} independent replica(s), no inter-GPU exchange",
@@ -655,7 +656,7 @@ def run_reference(args):
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate, bf16 I/O",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
         "data": "synthetic (seeded Irwin-Hall normal, sigma 1e-3)",
         "config": {"workload": WORKLOAD, "world": WORLD, "sample_elems_per_step": width},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
