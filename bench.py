@@ -489,6 +489,22 @@ def rows(peak):
         workload="402.8M W=8 bf16 as one bucket: relayout pass + ReduceScatter", launches=2)
     del g, parts, relaid, rs_out
 
+    # Accumulation on the 402.8M-parameter W=8 shape: bf16 micro-batch
+    # gradients into an fp32 [8, n] accumulator, one add and the fused finalize.
+    n = tree.total
+    acc8 = torch.empty((WORLD, n), dtype=torch.float32, device="cuda")
+    g8 = torch.empty((WORLD, n), dtype=torch.bfloat16, device="cuda")
+    datagen.fill_device(g8.data_ptr(), WORLD, n, n, BF16, NORMAL, SEED, 0, 1, 0, SIGMA, s)
+    zc.accumulate_microbatch(acc8, g8, first=True, finalize=False)
+    tot8 = torch.empty(n, dtype=torch.float32, device="cuda")
+    ms = timed(lambda: zc.accumulate_microbatch(acc8, g8, first=False, finalize=False), 5)
+    out["accumulate_402m_w8_add"] = entry(ms, WORLD * n * (4 + 2 + 4),
+                                          workload="402.8M W=8: fp32 acc += bf16 g (read acc, read g, write acc)")
+    ms = timed(lambda: zc.accumulate_microbatch(acc8, g8, first=False, finalize=True, total=tot8), 5)
+    out["accumulate_402m_w8_finalize"] = entry(ms, WORLD * n * (4 + 2) + 4 * n,
+                                               workload="402.8M W=8: last micro-batch fused with the reduce")
+    del acc8, g8, tot8
+
     # Deferred accumulation: W=4, 8 micro-batches, qwen3-0.6b tree, fp32.
     W, M = 4, 8
     n = workloads.tree_qwen3_06b().total

@@ -109,3 +109,31 @@ def test_step_captured_in_a_cuda_graph():
     for r in range(world):
         assert torch.equal(ex.grad.buf[r].view(torch.int16), fresh.buf[r].view(torch.int16))
     ex.close()
+
+
+def test_work_runs_on_the_callers_stream():
+    """Every entry point enqueues on the stream it is given: a flush on a side
+    stream that waits on an event sees gradients written just before that
+    event on another stream, and the default stream sees the flush's results
+    only after waiting on the side stream."""
+    world = 8
+    tree = workloads.straddle_tree(world, 30000 * world + 1, 3, pieces=3)
+    layout, grads, ex = _setup(world, tree, capacity=None)
+    ref = zc.GradBuffers(world, ex.omap, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+    b = layout.buckets[0]
+    zc.flush_bucket(grads, b.tasks, ex.omap.owner, ref.dst_table(b.tasks), BF16, True, True)
+    torch.cuda.synchronize()
+    for buf in ex.grad.buf:
+        buf.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    ready = torch.cuda.Event()
+    saved = grads.clone()
+    grads.zero_()                                   # default stream
+    grads.copy_(saved)
+    ready.record(torch.cuda.current_stream())
+    side.wait_event(ready)
+    ex.flush_all(grads, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    for r in range(world):
+        assert torch.equal(ex.grad.buf[r].view(torch.int16), ref.buf[r].view(torch.int16))
+    ex.close()
