@@ -120,6 +120,16 @@ int dpred_build_owner_map(int32_t world, int32_t rank, const dpred_group* groups
                           int32_t* n_owned, int32_t* n_total);
 
 /*
+ * Digest of an owner map (64-bit FNV-1a over n_params and the owner,
+ * holder_lo and holder_hi arrays, host).  [DS] "Design points": the map must
+ * be identical on every rank, because it decides which collective each bucket
+ * entry uses and every rank has to issue the same sequence.  Ranks exchange
+ * this digest to detect one built from inconsistent metadata before any flush.
+ */
+uint64_t dpred_owner_map_digest(int32_t n_params, const int32_t* owner, const int32_t* holder_lo,
+                                const int32_t* holder_hi);
+
+/*
  * The owner map of one parameter group, computed on the device (for an
  * executor whose parameter table lives in device memory).  Same rule and
  * results as dpred_build_owner_map for a single group: numel (device, int64

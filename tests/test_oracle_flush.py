@@ -290,3 +290,25 @@ def test_probe_owner_elems_excludes_straddlers():
         assert pr["owner_elems"] == pr["reduced_elems"] - strad
         total_owner += pr["owner_elems"]
     assert total_owner == 295_798_784
+
+
+def test_wrong_root_is_caught_vacuity_guard():
+    """A plausible mistake -- every owner shifted to the next rank -- changes
+    both the delivered buffers and the kept counts, so the parity checks that
+    compare them would fail on it."""
+    world = 4
+    tree, b, grads = _tiny(world)
+    om = oracle.owner_map(world, [(list(range(world)), tree.numel)], True)
+    holders = holder_sets(om["holder_lo"], om["holder_hi"])
+    right = oracle_dst(world, b.tasks, holders, True)
+    wrong = oracle_dst(world, b.tasks, holders, True)
+    bad_owner = np.where(om["owner"] >= 0, (om["owner"] + 1) % world, -1).astype(np.int32)
+    pr_right = oracle.flush(world, grads.copy(), b.tasks, om["owner"], tree.n_params, right, BF16, True, True)
+    oracle.flush(world, grads.copy(), b.tasks, bad_owner, tree.n_params, wrong, BF16, True, True)
+    differs = any(not np.array_equal(right[r][t], wrong[r][t])
+                  for r in range(world) for t in range(len(b.tasks)) if right[r][t] is not None)
+    assert differs
+    has = np.array([[right[r][t] is not None for t in range(len(b.tasks))] for r in range(world)])
+    assert oracle.flush_probe(world, b.tasks, bad_owner, tree.n_params, None, True)["kept_elems"] != \
+        oracle.flush_probe(world, b.tasks, om["owner"], tree.n_params, None, True)["kept_elems"]
+    assert pr_right["kept_elems"] == oracle.flush_probe(world, b.tasks, om["owner"], tree.n_params, has, True)["kept_elems"]

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.dpred_last_error.restype = ctypes.c_char_p
         L.dpred_version.restype = ctypes.c_char_p
         L.dpred_build_owner_map.argtypes = [i32, i32, vp, i32, i32, vp, vp, vp, vp, vp]
+        L.dpred_owner_map_digest.restype = ctypes.c_uint64
+        L.dpred_owner_map_digest.argtypes = [i32, vp, vp, vp]
         L.dpred_build_owner_map_device.argtypes = [i32, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp]
         L.dpred_flush_probe.argtypes = [i32, vp, i32, vp, i32, vp, i32, vp]
         L.dpred_flush_workspace_bytes.restype = ctypes.c_size_t
@@ -129,6 +131,12 @@ class OwnerMap:
     holder_hi: np.ndarray  # int32
     n_owned: int
     n_total: int
+
+    def digest(self) -> int:
+        """64-bit digest of the map (dpred_owner_map_digest), for cross-rank checks."""
+        n = len(self.owner)
+        return int(lib().dpred_owner_map_digest(n, self.owner.ctypes.data, self.holder_lo.ctypes.data,
+                                                self.holder_hi.ctypes.data))
 
     def report(self) -> str:
         """The init-time ratio report of the DeepSpeed issue (section "Additional context")."""

@@ -199,6 +199,23 @@ int dpred_build_owner_map(int32_t world, int32_t rank, const dpred_group* groups
     return DPRED_OK;
 }
 
+uint64_t dpred_owner_map_digest(int32_t n_params, const int32_t* owner, const int32_t* holder_lo,
+                                const int32_t* holder_hi) {
+    // FNV-1a (64-bit) over the parameter count and the three arrays, little-endian
+    uint64_t h = 0xcbf29ce484222325ull;
+    auto mix = [&h](uint32_t v) {
+        for (int b = 0; b < 4; ++b) {
+            h ^= (v >> (8 * b)) & 0xffu;
+            h *= 0x100000001b3ull;
+        }
+    };
+    mix((uint32_t)n_params);
+    const int32_t* arrays[3] = {owner, holder_lo, holder_hi};
+    for (const int32_t* a : arrays)
+        for (int32_t i = 0; a && i < n_params; ++i) mix((uint32_t)a[i]);
+    return h;
+}
+
 static int validate_tasks(int32_t world, const dpred_task* tasks, int32_t n_tasks, const int32_t* owner,
                           int32_t n_params, int64_t ld, bool check_ld) {
     if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
