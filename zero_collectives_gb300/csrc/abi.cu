@@ -28,6 +28,7 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     const bool rows_vec = reinterpret_cast<uintptr_t>(grads) % 16 == 0 && (ld * isz) % 16 == 0;
     out.tasks.clear();
     out.pool.clear();
+    out.realign = false;
     out.tasks.reserve(tasks.size());
     int64_t units = 0;
     const int unit_vec = kUnitVec * flush_batch(world);
@@ -43,8 +44,27 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
         bool vec = rows_vec;
         for (void* p : d.ptrs)
             if ((reinterpret_cast<uintptr_t>(p) + (uintptr_t)head * osz) % out_align != 0) vec = false;
-        t.vec = vec ? 1 : 0;
-        t.head = vec ? (uint8_t)head : 0;
+        int mode = vec ? 1 : 0;
+        if (!vec && rows_vec && in_dt == out_dt && (d.numel - head) / vec_elems >= 2) {
+            // Same element type, destinations shifted against the source grid:
+            // the realigned vector path when every destination has the same shift.
+            int sigma = -1;
+            for (void* p : d.ptrs) {
+                const int64_t de = (int64_t)(reinterpret_cast<uintptr_t>(p) / (uintptr_t)osz);
+                const int64_t a = (vec_elems - de % vec_elems) % vec_elems;  // first 16-byte aligned element
+                const int sg = (int)(((head - a) % vec_elems + vec_elems) % vec_elems);
+                if (sigma < 0) {
+                    sigma = sg;
+                } else if (sg != sigma) {
+                    sigma = 0;
+                    break;
+                }
+            }
+            if (sigma > 0) mode = 1 + sigma;
+        }
+        t.vec = (uint8_t)mode;
+        t.head = mode ? (uint8_t)head : 0;
+        if (mode >= 2) out.realign = true;
         t.unit_begin = units;
         units += flush_task_units(t, vec_elems, unit_vec);
         out.pool.insert(out.pool.end(), d.ptrs.begin(), d.ptrs.end());
@@ -76,6 +96,7 @@ int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cud
     L.n_dst = (int)p.pool.size();
     L.workspace = workspace;
     L.workspace_bytes = workspace_bytes;
+    L.realign = p.realign;
     return p.in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
 }
 

@@ -80,7 +80,7 @@ struct TaskDesc {
     int64_t unit_begin;  // first work unit of the task (prefix over the plan)
     int32_t dst_begin;   // first destination pointer in the plan's pointer pool
     int16_t ndst;        // destinations to write (0..world)
-    uint8_t vec;         // 1: 16-byte vector path (rows and destinations co-aligned)
+    uint8_t vec;         // 0 scalar; 1 16-byte vectors, destinations co-aligned; 1+s realigned by s elements
     uint8_t head;        // scalar elements before the first 16-byte aligned vector
 };
 static_assert(sizeof(TaskDesc) == 32, "TaskDesc layout");
@@ -127,6 +127,7 @@ struct FlushLaunch {
     int n_dst;
     void* workspace;         // device, used when the plan does not fit inline
     size_t workspace_bytes;
+    bool realign;            // some task takes the realigned vector path
 };
 
 // Vectors each thread keeps in flight per replica row: small world sizes take
@@ -153,6 +154,7 @@ struct Dest {
 struct BuiltPlan {
     FlushHeader h;
     int in_dt, out_dt;
+    bool realign = false;
     std::vector<TaskDesc> tasks;
     std::vector<void*> pool;
 };

@@ -18,6 +18,8 @@
 // loads in flight, then reduces them in rank order.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "tma.cuh"
 
@@ -169,10 +171,163 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
     }
 }
 
-template <int W_T, int BATCH, typename Tin, typename Tout, int MODE, typename Args>
+// ---------------------------------------------------------------------------
+// Realigned vector path: the task's destinations are not co-aligned with its
+// source (same element type, destination start shifted by sigma elements
+// against the 16-byte grid of the source).  Loads stay source-aligned; each
+// thread packs its vector v, takes vector v-1's packed result from the lane
+// to its left (lane 0 recomputes it), and stores the destination-aligned
+// 16 bytes made of the last sigma elements of v-1 and the first VEC-sigma of v.
+
+template <typename T>
+__device__ __forceinline__ uint4 pack_vec(const float (&y)[Elem<T>::kVec]);
+template <>
+__device__ __forceinline__ uint4 pack_vec<__nv_bfloat16>(const float (&y)[8]) {
+    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                      pack_bf16x2(y[6], y[7]));
+}
+template <>
+__device__ __forceinline__ uint4 pack_vec<float>(const float (&y)[4]) {
+    return make_uint4(__float_as_uint(y[0]), __float_as_uint(y[1]), __float_as_uint(y[2]), __float_as_uint(y[3]));
+}
+
+// Elements [VEC - S, 2 VEC - S) of the element stream P ++ C (S in 1..VEC-1).
+template <typename T, int S>
+__device__ __forceinline__ uint4 shifted(const uint4& P, const uint4& C) {
+    const uint32_t E[8] = {P.x, P.y, P.z, P.w, C.x, C.y, C.z, C.w};
+    uint32_t w[4];
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        constexpr int o = 8 - S;  // element offset, two elements per word
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if constexpr (o % 2 == 0)
+                w[i] = E[o / 2 + i];
+            else
+                w[i] = __byte_perm(E[o / 2 + i], E[o / 2 + i + 1], 0x5432);
+        }
+    } else {
+        constexpr int o = 4 - S;  // one element per word
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = E[o + i];
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 shifted_rt(int s, const uint4& P, const uint4& C) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        switch (s) {
+            case 1: return shifted<T, 1>(P, C);
+            case 2: return shifted<T, 2>(P, C);
+            case 3: return shifted<T, 3>(P, C);
+            case 4: return shifted<T, 4>(P, C);
+            case 5: return shifted<T, 5>(P, C);
+            case 6: return shifted<T, 6>(P, C);
+            default: return shifted<T, 7>(P, C);
+        }
+    } else {
+        switch (s) {
+            case 1: return shifted<T, 1>(P, C);
+            case 2: return shifted<T, 2>(P, C);
+            default: return shifted<T, 3>(P, C);
+        }
+    }
+}
+
+// Reduced, packed source vector v of the task (rows in rank order).
+template <int W_T, typename T, int MODE>
+__device__ __forceinline__ uint4 reduce_packed(const uint4* base, int64_t stride, int64_t v, int world, float wf,
+                                               float inv_w) {
+    constexpr int VEC = Elem<T>::kVec;
+    float y[VEC];
+    if constexpr (W_T > 0) {
+        uint4 q[W_T];
+#pragma unroll
+        for (int r = 0; r < W_T; ++r) q[r] = __ldcs(base + r * stride + v);
+#pragma unroll
+        for (int r = 0; r < W_T; ++r) fold<T, MODE>(y, q[r], r == 0, wf, inv_w);
+    } else {
+        for (int r = 0; r < world; ++r) fold<T, MODE>(y, __ldcs(base + (int64_t)r * stride + v), r == 0, wf, inv_w);
+    }
+    return pack_vec<T>(y);
+}
+
+// Barrier over the kFlushThreads threads that reduce (id 1; in the TMA kernel
+// the producer thread never reaches it).
+__device__ __forceinline__ void reducers_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"r"(kFlushThreads) : "memory");
+}
+
+// Vectors [v0, v1) of the task's source body, one per thread per pass.  A
+// thread takes vector v-1's packed result from the lane to its left, lane 0
+// of a warp from lane 31 of the warp before it (shared memory), and thread 0
+// from the last thread of the previous pass.  The output that straddles the
+// unit's first vector and the previous unit is written on the scalar path by
+// the caller.  Passes are uniform across the block so that every thread takes
+// part in the shuffles and barriers; out-of-range threads re-read vector v1-1
+// and store nothing.
+template <int W_T, typename T, int MODE, typename Args>
+__device__ __forceinline__ void flush_unit_realign(const Args& a, const TaskDesc& Tk, int64_t v0, int64_t v1,
+                                                   int sigma) {
+    constexpr int VEC = Elem<T>::kVec;
+    __shared__ uint4 s_last[kFlushThreads / 32];
+    __shared__ uint4 s_carry;
+    const FlushHeader& h = a.h;
+    const int64_t stride = h.ld / VEC;
+    const uint4* base = reinterpret_cast<const uint4*>(static_cast<const T*>(h.grads) + Tk.src_off + Tk.head);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    for (int64_t pb = v0; pb < v1; pb += kFlushThreads) {
+        const int64_t v = pb + t;
+        const int64_t vl = v < v1 ? v : v1 - 1;
+        const uint4 C = reduce_packed<W_T, T, MODE>(base, stride, vl, h.world, h.wf, h.inv_w);
+        uint4 P;
+        P.x = __shfl_up_sync(0xffffffffu, C.x, 1);
+        P.y = __shfl_up_sync(0xffffffffu, C.y, 1);
+        P.z = __shfl_up_sync(0xffffffffu, C.z, 1);
+        P.w = __shfl_up_sync(0xffffffffu, C.w, 1);
+        if (lane == 31) s_last[warp] = C;
+        reducers_barrier();
+        if (lane == 0) P = warp > 0 ? s_last[warp - 1] : s_carry;  // s_carry: set by the previous pass
+        reducers_barrier();
+        if (t == kFlushThreads - 1) s_carry = C;
+        if (v > v0 && v < v1) {
+            const uint4 out = shifted_rt<T>(sigma, P, C);
+            const int64_t e = Tk.head + v * VEC - sigma;  // destination-aligned element index
+            for (int d = 0; d < Tk.ndst; ++d)
+                __stcs(reinterpret_cast<uint4*>(static_cast<T*>(plan_dst(a, Tk.dst_begin + d)) + e), out);
+        }
+    }
+}
+
+// Unit of a realigned task: its vectors, plus (in unit 0) the scalar head
+// [0, head + VEC - sigma) and tail [head + VEC * nbody - sigma, numel).
+template <int W_T, typename Tin, typename Tout, int MODE, typename Args>
+__device__ __forceinline__ void flush_unit_shifted(const Args& a, const TaskDesc& T, int64_t local, int threads) {
+    if constexpr (std::is_same<Tin, Tout>::value) {
+        constexpr int VEC = Elem<Tin>::kVec;
+        const int sigma = T.vec - 1;
+        const int64_t nbody = (T.numel - T.head) / VEC;
+        const int64_t v0 = local * (int64_t)a.h.unit_vec;
+        const int64_t v1 = v0 + a.h.unit_vec < nbody ? v0 + a.h.unit_vec : nbody;
+        flush_unit_realign<W_T, Tin, MODE>(a, T, v0, v1, sigma);
+        // the destination vector that straddles vector v0-1 and v0 (another unit)
+        if (v0 >= 1 && (int)threadIdx.x < VEC) flush_element<Tin, Tout, MODE>(a, T, T.head + v0 * VEC - sigma + threadIdx.x);
+        if (local == 0) {
+            const int hcount = T.head + VEC - sigma;
+            const int64_t tstart = T.head + nbody * VEC - sigma;
+            const int tcount = (int)(T.numel - tstart);
+            for (int id = threadIdx.x; id < hcount + tcount; id += threads)
+                flush_element<Tin, Tout, MODE>(a, T, id < hcount ? id : tstart + (id - hcount));
+        }
+    }
+}
+
+template <int W_T, int BATCH, typename Tin, typename Tout, int MODE, bool RA, typename Args>
 __device__ __forceinline__ void flush_unit(const Args& a, const TaskDesc& T, int64_t local) {
     constexpr int VEC = Elem<Tin>::kVec;
-    if (T.vec) {
+    if (RA && T.vec >= 2) {
+        if constexpr (RA) flush_unit_shifted<W_T, Tin, Tout, MODE>(a, T, local, kFlushThreads);
+    } else if (T.vec) {
         const int64_t nbody = (T.numel - T.head) / VEC;
         const int64_t v0 = local * h_unit(a);
         const int64_t v1 = v0 + h_unit(a) < nbody ? v0 + h_unit(a) : nbody;
@@ -206,18 +361,21 @@ __device__ __forceinline__ int find_task(const Args& a, int64_t u) {
     return lo;
 }
 
-template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
+// RA: the plan holds realigned tasks (destinations shifted against the
+// source).  That path is compiled into its own kernel so that the common
+// kernel keeps its register budget.
+template <int W_T, int BATCH, typename Tin, typename Tout, typename Args, bool RA>
 __global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_constant__ Args a) {
     const FlushHeader& h = a.h;
     for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
         const TaskDesc T = plan_task(a, find_task(a, u));
         const int64_t local = u - T.unit_begin;
         if (h.pdiv == PDIV_POW2)
-            flush_unit<W_T, BATCH, Tin, Tout, PDIV_POW2>(a, T, local);
+            flush_unit<W_T, BATCH, Tin, Tout, PDIV_POW2, RA>(a, T, local);
         else if (h.pdiv == PDIV_DIV)
-            flush_unit<W_T, BATCH, Tin, Tout, PDIV_DIV>(a, T, local);
+            flush_unit<W_T, BATCH, Tin, Tout, PDIV_DIV, RA>(a, T, local);
         else
-            flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE>(a, T, local);
+            flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE, RA>(a, T, local);
     }
 }
 
@@ -272,6 +430,10 @@ __device__ void tma_consume(const Args& a, unsigned char* smem, uint64_t* full, 
             for (int64_t k = e0 + ctid; k < e1; k += kTmaConsumers) flush_element<Tin, Tout, MODE>(a, T, k);
             continue;
         }
+        if (T.vec >= 2) {  // destinations shifted against the source: register path, no staging
+            flush_unit_shifted<W_T, Tin, Tout, MODE>(a, T, local, kTmaConsumers);
+            continue;
+        }
         const int64_t nbody = (T.numel - T.head) / VEC;
         const int64_t v0 = local * (int64_t)h.unit_vec;
         const int64_t v1 = v0 + h.unit_vec < nbody ? v0 + h.unit_vec : nbody;
@@ -322,7 +484,7 @@ __device__ void tma_produce(const Args& a, unsigned char* smem, uint64_t* full, 
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < h.total_units; u += gridDim.x) {
         const TaskDesc T = plan_task(a, find_task(a, u));
-        if (!T.vec) continue;
+        if (T.vec != 1) continue;  // only co-aligned vector tasks are staged
         const int64_t local = u - T.unit_begin;
         const int64_t nbody = (T.numel - T.head) / VEC;
         const int64_t v0 = local * (int64_t)h.unit_vec;
@@ -402,7 +564,7 @@ int64_t persistent_grid(K kernel, int64_t units) {
 // One launch of the LDG kernel (any W) or, for W in {2, 4, 8, 16} when the
 // TMA path is selected, of the TMA-staged kernel (one CTA per SM).
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
-cudaError_t launch_kernel(const Args& a, int64_t units, cudaStream_t s) {
+cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, cudaStream_t s) {
     if constexpr (W_T > 0) {
         if (flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
             auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
@@ -415,7 +577,14 @@ cudaError_t launch_kernel(const Args& a, int64_t units, cudaStream_t s) {
             return cudaGetLastError();
         }
     }
-    auto k = flush_kernel<W_T, BATCH, Tin, Tout, Args>;
+    if constexpr (std::is_same<Tin, Tout>::value) {
+        if (realign) {
+            auto k = flush_kernel<W_T, BATCH, Tin, Tout, Args, true>;
+            k<<<(unsigned)persistent_grid(k, units), kFlushThreads, 0, s>>>(a);
+            return cudaGetLastError();
+        }
+    }
+    auto k = flush_kernel<W_T, BATCH, Tin, Tout, Args, false>;
     k<<<(unsigned)persistent_grid(k, units), kFlushThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
@@ -430,7 +599,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         for (int i = 0; i < h.n_tasks; ++i) a.tasks[i] = L.tasks[i];
         for (int i = 0; i < L.n_dst; ++i) a.dst[i] = L.dst[i];
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, s);
     } else {
         size_t tb = sizeof(TaskDesc) * (size_t)h.n_tasks, db = sizeof(void*) * (size_t)L.n_dst;
         size_t need = tb + ((db + 15) & ~(size_t)15);
@@ -447,7 +616,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         a.tasks = reinterpret_cast<const TaskDesc*>(ws);
         a.dst = reinterpret_cast<void* const*>(ws + tb);
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, s);
     }
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
 }
