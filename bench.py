@@ -292,7 +292,7 @@ def run_dpred(args):
         "algorithmic_bytes_per_step": step_bytes,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_src,
-                     "kernel": "flush_kernel<8,1,bf16,bf16,FlushArgsInline>", "bytes_per_launch": bytes_per_launch,
+                     "kernel": "flush_kernel<8,1,bf16,bf16,FlushArgsInline,false>", "bytes_per_launch": bytes_per_launch,
                      "avg_launch_ms": round(avg_launch_ms, 5)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
