@@ -244,3 +244,30 @@ def test_executor_create_validates_and_destroys_without_a_gpu(L):
     assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, 0x10000, 128, 1, starts.ctypes.data,
                                    counts.ctypes.data, tasks.ctypes.data, None, None, 0, ctypes.byref(h)) == -1
     assert L.dpred_executor_flush(None, 0, None, None) == -1
+
+
+def test_flush_path_and_pipeline_argument_errors(L):
+    with pytest.raises(zc.DpredError):
+        zc.set_flush_path(7)
+    prev = zc.set_flush_path(zc.PATH_LDG)
+    assert zc.set_flush_path(prev) == zc.PATH_LDG
+    # the host pipeline rejects bad arguments before touching any stream
+    world = 2
+    tasks = _tasks([(0, 0, 32)])
+    owner = np.array([0], np.int32)
+    starts = np.array([0], np.int64)
+    counts = np.array([1], np.int32)
+    dst = (ctypes.c_void_p * 2)(0x200000, None)
+    h = ctypes.c_void_p()
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 1, 0x10000, 64, 1, starts.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == 0
+    reg_dev = (ctypes.c_void_p * 1)(0x200000)
+    reg_host = (ctypes.c_void_p * 1)(0x300000)
+    nbytes = np.array([64], np.int64)
+    assert L.dpred_executor_flush_all_from_host(h, None, 64, 1, reg_dev, reg_host, nbytes.ctypes.data, None,
+                                                None) == -1                     # no host gradients
+    small = np.array([16], np.int64)                                            # destination outside every region
+    assert L.dpred_executor_flush_all_from_host(h, 0x400000, 64, 1, reg_dev, reg_host, small.ctypes.data, None,
+                                                None) == -1
+    assert L.dpred_executor_flush(h, 3, None, None) == -1                      # bucket out of range
+    assert L.dpred_executor_destroy(h) == 0
