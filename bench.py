@@ -297,6 +297,17 @@ def run_dpred(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
+    # Step-time distribution: a separate pass with one event pair per step (the
+    # headline region above has no per-step events).
+    evs = events(51)
+    evs[0].record(stream)
+    for i in range(50):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(50))
+    result["step_ms_p10_p50_p90"] = [round(per[5], 4), round(per[25], 4), round(per[45], 4)]
+    result["replica_elems_per_s"] = round(elems_per_s * WORLD, 1)
     probe_line = ex.flush_all(grads, probe=True)[0].line(0, zc.BF16, True)
     result["probe_line"] = probe_line
     result["owner_map_report"] = ex.omap.report()
