@@ -316,6 +316,7 @@ def run_dpred(args):
         result["e2e"] = e2e(args, ex, grads, step_bytes, ws)
     if rank == 0 and not args.no_cpu:
         result["cpu_baseline"] = cpu_baseline(buckets, tree, layout, args.cpu_seconds)
+        result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(buckets, tree)
     if not args.no_rows:
         result["flush_paths"] = flush_path_ab(ex, grads, step_bytes, peak)
         del grads
@@ -400,6 +401,76 @@ def cpu_baseline(buckets, tree, layout, seconds):
     return {"value": round(nbytes / secs / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"{nb} of {len(buckets)} buckets ({elems} elements per replica row), single-threaded C oracle",
             "seconds": round(secs, 2), "grad_elems_per_s": round(elems / secs, 1)}
+
+
+def _cpu_worker(job):
+    """One host core: the unchanged single-threaded oracle on a contiguous run of
+    bucket 0's tasks, repeated until `seconds` have passed.  Runs in a spawned
+    process; the start barrier lines all workers up before anyone times."""
+    import numpy as np
+    import datagen
+    import oracle
+    from datagen import BF16, NORMAL
+    tasks, col0, n_params, numel, seconds, barrier = job
+    om = oracle.owner_map(WORLD, [(list(range(WORLD)), numel)], True)
+    base = int(tasks["offset"][0])
+    tasks = tasks.copy()
+    tasks["offset"] -= base
+    width = int(tasks["offset"][-1] + tasks["numel"][-1])
+    host = datagen.host_matrix(WORLD, width, BF16, NORMAL, SEED, col0=col0 + base, sigma=SIGMA)
+    dst = [[None] * len(tasks) for _ in range(WORLD)]
+    writes = 0
+    for t, task in enumerate(tasks):
+        p = int(task["param_id"])
+        lo, hi = int(om["holder_lo"][p]), int(om["holder_hi"][p])
+        for r in range(lo, hi + 1):
+            dst[r][t] = np.empty(int(task["numel"]), np.uint16)
+        writes += int(task["numel"]) * (1 if om["owner"][p] >= 0 else hi - lo + 1)
+    per_pass = WORLD * width * 2 + writes * 2
+    barrier.wait()
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.flush(WORLD, host, tasks, om["owner"], n_params, dst, BF16, True, True)
+        passes += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return t0, time.perf_counter(), passes * per_pass
+
+
+def cpu_baseline_all_cores(buckets, tree, seconds=1.5):
+    """The same single-threaded oracle run as one process per host core, each on
+    its own contiguous share of bucket 0's tasks, all started together.  The
+    figure is the bytes of all workers over the wall time from the first start
+    to the last finish."""
+    import multiprocessing as mp
+    cores = len(os.sched_getaffinity(0))
+    b = buckets[0]
+    cum = [0]
+    for t in b.tasks:
+        cum.append(cum[-1] + int(t["numel"]))
+    groups, start = [], 0
+    for c in range(1, cores + 1):
+        target = b.size * c // cores
+        end = start
+        while end < len(b.tasks) and cum[end + 1] <= target:
+            end += 1
+        if c == cores:
+            end = len(b.tasks)
+        if end > start:
+            groups.append(b.tasks[start:end])
+        start = end
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        barrier = mgr.Barrier(len(groups))
+        with ctx.Pool(len(groups)) as pool:
+            res = pool.map(_cpu_worker, [(g, b.start, tree.n_params, tree.numel, seconds, barrier) for g in groups])
+    wall = max(r[1] for r in res) - min(r[0] for r in res)
+    nbytes = sum(r[2] for r in res)
+    return {"value": round(nbytes / wall / 1e9, 3), "unit": "GB/s", "cores": len(groups), "kind": "oracle",
+            "sample": f"bucket 0 ({b.size} elements per replica row) split by tasks over {len(groups)} processes, "
+                      f"each the single-threaded C oracle repeated for {seconds} s",
+            "seconds": round(wall, 2)}
 
 
 def flush_path_ab(ex, grads, step_bytes, peak):
