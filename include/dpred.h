@@ -259,6 +259,19 @@ int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int
  *     leave as soon as it is done); `stream` waits for its earlier work first
  *     and finishes after the last copy.  The first call creates the streams
  *     and events.  Not re-entrant for one executor.
+ *   dpred_executor_flush_all_mapped: the same step with the same arguments:
+ *     every destination byte a flush writes lands at the same place in the
+ *     host regions (host bytes no destination covers stay untouched).  But
+ *     nothing is staged in device memory: the flush kernels read the bucket
+ *     columns of host_grads and
+ *     write the reduced gradients into the host regions directly, over the
+ *     host link (the memory must be pinned and mapped, see
+ *     dpred_host_mapped_pointer).  grads and the device regions are neither
+ *     read nor written; the device regions only say where in the host
+ *     regions each result goes.  One launch per bucket on `stream`, in order;
+ *     no extra streams.  The plans for a set of host pointers are built on
+ *     the first call that uses them and reused while they stay the same.
+ *     host_ld must cover every bucket's columns (DPRED_E_SIZE).
  *   dpred_executor_destroy:   release the executor (after its work is done).
  */
 typedef struct dpred_executor dpred_executor;
@@ -271,6 +284,9 @@ int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stre
 int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
                                        void* const* region_dev, void* const* region_host, const int64_t* region_bytes,
                                        dpred_probe* probes, void* stream);
+int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
+                                    void* const* region_dev, void* const* region_host, const int64_t* region_bytes,
+                                    dpred_probe* probes, void* stream);
 int dpred_executor_destroy(dpred_executor* ex);
 
 /*
@@ -444,6 +460,17 @@ int dpred_allgather_schedule_step(int32_t schedule, int32_t n_nodes, int64_t sha
  * the last clear.  Synchronises the current device.  clear != 0 resets it.
  */
 int dpred_device_status(int32_t* code, int32_t clear);
+
+/*
+ * The device address of page-locked (pinned) host memory, for kernels that
+ * read or write host buffers directly over the host link (no counterpart in
+ * the pages).  host: any address inside a pinned allocation (cudaHostAlloc,
+ * or cudaHostRegister with mapping).  *dev receives the address the current
+ * device uses for the same byte; with unified addressing it equals host.
+ * Errors: DPRED_E_INVAL (null, or memory that is not pinned and mapped),
+ * DPRED_E_CUDA.  Synchronous; enqueues nothing.
+ */
+int dpred_host_mapped_pointer(const void* host, void** dev);
 
 /*
  * Self-test of the bounded-wait path (no counterpart in the pages): launches

@@ -46,8 +46,9 @@ def test_executor_equals_single_calls(world):
     ex.close()
 
 
+@pytest.mark.parametrize("mode", ["from_host", "mapped"])
 @pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
-def test_host_buffer_step_matches_device_path(dt):
+def test_host_buffer_step_matches_device_path(dt, mode):
     world = 8
     tree = workloads.straddle_tree(world, 300000 * world + 5, 5, pieces=4)
     code = BF16 if dt == torch.bfloat16 else F32
@@ -62,11 +63,18 @@ def test_host_buffer_step_matches_device_path(dt):
     scratch = torch.zeros_like(grads_dev)
     ex2 = zc.Zero1Executor(world, tree.numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets], dt,
                            fill=float("nan"))
-    for _ in range(2):   # twice in a row: the pipeline's events and streams are reused
+    for _ in range(2):   # twice in a row: the pipeline's streams, or the mapped plans, are reused
         for o in outs:
             o.fill_(float("nan"))
-        ex2.flush_all_from_host(host, outs, scratch)
+        if mode == "from_host":
+            ex2.flush_all_from_host(host, outs, scratch)
+        else:
+            ex2.flush_all_mapped(host, outs, scratch)
         torch.cuda.synchronize()
+        if mode == "mapped":
+            # nothing was staged: the device gradients and buffers were not touched
+            assert not scratch.any()
+            assert all(torch.isnan(b.float()).all() for b in ex2.grad.buf)
         for r in range(world):
             # everything a bucket wrote came back; the rest of the host buffer is untouched (NaN)
             w = want[r].cpu()
@@ -136,4 +144,25 @@ def test_work_runs_on_the_callers_stream():
     torch.cuda.current_stream().wait_stream(side)
     for r in range(world):
         assert torch.equal(ex.grad.buf[r].view(torch.int16), ref.buf[r].view(torch.int16))
+    ex.close()
+
+
+def test_mapped_step_rejects_pageable_host_memory():
+    world = 4
+    tree = workloads.straddle_tree(world, 5000 * world + 1, 2, pieces=2)
+    layout, grads, ex = _setup(world, tree, capacity=tree.total // 2)
+    pinned = torch.zeros((world, tree.total), dtype=torch.bfloat16, pin_memory=True)
+    pageable = torch.zeros((world, tree.total), dtype=torch.bfloat16)
+    outs = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in ex.grad.buf]
+    with pytest.raises(zc.DpredError) as e:
+        ex.flush_all_mapped(pageable, outs, grads)
+    assert e.value.code == -1                     # DPRED_E_INVAL
+    with pytest.raises(zc.DpredError) as e:
+        ex.flush_all_mapped(pinned, [torch.empty(b.shape, dtype=b.dtype) for b in ex.grad.buf], grads)
+    assert e.value.code == -1
+    short = torch.zeros((world, tree.total // 2), dtype=torch.bfloat16, pin_memory=True)
+    with pytest.raises(zc.DpredError) as e:       # rows shorter than the buckets span
+        ex.flush_all_mapped(short, outs, grads)
+    assert e.value.code == -3                     # DPRED_E_SIZE
+    assert zc.host_mapped_pointer(pinned) != 0
     ex.close()

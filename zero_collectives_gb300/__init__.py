@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
         L.dpred_device_status.argtypes = [vp, i32]
         L.dpred_set_flush_path.argtypes = [i32]
         L.dpred_selftest_wait_timeout.argtypes = [i64, vp]
+        L.dpred_host_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
+        L.dpred_executor_flush_all_mapped.argtypes = L.dpred_executor_flush_all_from_host.argtypes
         _lib = L
     return _lib
 
@@ -481,6 +483,14 @@ def device_status(clear: bool = False) -> int:
     return code.value
 
 
+def host_mapped_pointer(t) -> int:
+    """Device address of a pinned host tensor's first element (the address a
+    kernel uses to read or write it over the host link)."""
+    out = ctypes.c_void_p()
+    _check(lib().dpred_host_mapped_pointer(t.data_ptr(), ctypes.byref(out)))
+    return int(out.value or 0)
+
+
 # ------------------------------------------------------- gradient buffers ---
 
 class GradBuffers:
@@ -656,4 +666,25 @@ class Zero1Executor:
         hld = host_grads.stride(0) if W > 1 else host_grads.shape[1]
         _check(lib().dpred_executor_flush_all_from_host(self._native, host_grads.data_ptr(), hld, W, dev, host,
                                                         nbytes.ctypes.data, probes, _stream(stream)))
+        return self._finish(probes, probe)
+
+    def flush_all_mapped(self, host_grads, host_bufs, grads, stream=None, probe: bool = False):
+        """The host-buffer step without staging: the flush kernels read
+        host_grads (pinned [W, n]) and write each rank's reduced gradients into
+        host_bufs[r] (pinned, laid out like that rank's device buffer) over the
+        host link.  grads and the device buffers are not touched."""
+        self._bind(grads)
+        W = self.world
+        if len(host_bufs) != W:
+            raise ValueError("one host buffer per rank")
+        for h, b in zip(host_bufs, self.grad.buf):
+            if h.numel() * h.element_size() < b.numel() * b.element_size():
+                raise ValueError("host buffer smaller than its device buffer")
+        dev = (ctypes.c_void_p * W)(*[b.data_ptr() for b in self.grad.buf])
+        host = (ctypes.c_void_p * W)(*[h.data_ptr() for h in host_bufs])
+        nbytes = np.array([b.numel() * b.element_size() for b in self.grad.buf], np.int64)
+        probes = self._probes(probe or self.probe_log is not None)
+        hld = host_grads.stride(0) if W > 1 else host_grads.shape[1]
+        _check(lib().dpred_executor_flush_all_mapped(self._native, host_grads.data_ptr(), hld, W, dev, host,
+                                                     nbytes.ctypes.data, probes, _stream(stream)))
         return self._finish(probes, probe)

@@ -97,6 +97,7 @@ int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cud
     L.workspace = workspace;
     L.workspace_bytes = workspace_bytes;
     L.realign = p.realign;
+    L.ldg_only = p.ldg_only;
     return p.in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
 }
 

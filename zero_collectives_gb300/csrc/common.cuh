@@ -128,6 +128,7 @@ struct FlushLaunch {
     void* workspace;         // device, used when the plan does not fit inline
     size_t workspace_bytes;
     bool realign;            // some task takes the realigned vector path
+    bool ldg_only;           // register streaming only: an operand lives in host memory
 };
 
 // Vectors each thread keeps in flight per replica row: small world sizes take
@@ -155,6 +156,7 @@ struct BuiltPlan {
     FlushHeader h;
     int in_dt, out_dt;
     bool realign = false;
+    bool ldg_only = false;  // gradients or destinations in pinned host memory
     std::vector<TaskDesc> tasks;
     std::vector<void*> pool;
 };

@@ -25,13 +25,17 @@
 #include "common.cuh"
 
 struct dpred_executor {
-    int world, in_dt, out_dt;
+    int world, in_dt, out_dt, pre_div;
     const char* grads;  // device [world, ld]
     int64_t ld;
     std::vector<int64_t> start, size;             // per bucket: column range of the gradient rows
     std::vector<dpred::BuiltPlan> plans;          // per bucket
     std::vector<dpred_probe> probes;              // per bucket (flush_index filled per call)
     std::vector<std::vector<std::pair<char*, int64_t>>> written;  // per bucket: [device pointer, bytes] written
+    std::vector<std::vector<dpred::Dest>> dests;  // per bucket: the delivered destinations the plan was built from
+    // plans of the mapped host step, rebuilt when its host pointers change
+    std::vector<dpred::BuiltPlan> mapped;
+    std::vector<const void*> mapped_key;
     void* workspace;
     size_t workspace_bytes;
     int64_t flushes = 0;
@@ -81,6 +85,22 @@ void release(dpred_executor* ex) {
 
 extern "C" {
 
+int dpred_host_mapped_pointer(const void* host, void** dev) {
+    using namespace dpred;
+    if (!host || !dev) return set_error(DPRED_E_INVAL, "null pointer");
+    *dev = nullptr;
+    cudaPointerAttributes a{};
+    const cudaError_t e = cudaPointerGetAttributes(&a, host);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return cuda_error(e, "cudaPointerGetAttributes");
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr)
+        return set_error(DPRED_E_INVAL, "%p is not page-locked host memory mapped into the device address space", host);
+    *dev = a.devicePointer;
+    return DPRED_OK;
+}
+
 int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div, int32_t reduce_to_owner,
                           const int32_t* owner, int32_t n_params, const void* grads, int64_t ld, int32_t n_buckets,
                           const int64_t* bucket_start, const int32_t* bucket_tasks, const dpred_task* tasks,
@@ -96,6 +116,7 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
     ex->world = world;
     ex->in_dt = in_dtype;
     ex->out_dt = out_dtype;
+    ex->pre_div = pre_div;
     ex->grads = static_cast<const char*>(grads);
     ex->ld = ld;
     ex->workspace = workspace;
@@ -164,6 +185,7 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
         ex->plans.push_back(std::move(bp));
         ex->probes.push_back(pr);
         ex->written.push_back(std::move(wr));
+        ex->dests.push_back(std::move(plan));
         t0 += nt;
         d0 += (int64_t)world * nt;
     }
@@ -261,6 +283,75 @@ int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grad
     if (e == cudaSuccess) e = cudaEventRecord(ex->ev_done, ex->d2h);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ex->ev_done, 0);  // the caller's stream completes last
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "executor host pipeline");
+}
+
+int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
+                                    void* const* region_dev, void* const* region_host, const int64_t* region_bytes,
+                                    dpred_probe* probes, void* stream) {
+    using namespace dpred;
+    if (!ex) return set_error(DPRED_E_INVAL, "null executor");
+    if (!host_grads || host_ld < 0) return set_error(DPRED_E_INVAL, "bad host gradients");
+    if (reinterpret_cast<uintptr_t>(host_grads) % esz(ex->in_dt))
+        return set_error(DPRED_E_ALIGN, "host gradients not aligned to their element size");
+    if (n_regions < 0 || (n_regions > 0 && (!region_dev || !region_host || !region_bytes)))
+        return set_error(DPRED_E_INVAL, "bad output regions");
+    int64_t width = 0;
+    for (size_t b = 0; b < ex->plans.size(); ++b) width = std::max(width, ex->start[b] + ex->size[b]);
+    if (host_ld < width)
+        return set_error(DPRED_E_SIZE, "host rows of %lld elements, the buckets span %lld", (long long)host_ld,
+                         (long long)width);
+    std::lock_guard<std::mutex> lock(ex->mu);
+    std::vector<const void*> key{host_grads, reinterpret_cast<const void*>(host_ld)};
+    for (int i = 0; i < n_regions; ++i) {
+        key.push_back(region_dev[i]);
+        key.push_back(region_host[i]);
+        key.push_back(reinterpret_cast<const void*>(region_bytes[i]));
+    }
+    if (key != ex->mapped_key) {
+        void* gdev = nullptr;
+        int rc = dpred_host_mapped_pointer(host_grads, &gdev);
+        if (rc) return rc;
+        std::vector<char*> hdev(n_regions, nullptr);
+        for (int i = 0; i < n_regions; ++i) {
+            if (region_bytes[i] < 0) return set_error(DPRED_E_INVAL, "region %d: negative size", i);
+            if (region_bytes[i] == 0) continue;
+            void* d = nullptr;
+            rc = dpred_host_mapped_pointer(region_host[i], &d);
+            if (rc) return rc;
+            hdev[i] = static_cast<char*>(d);
+        }
+        const int osz = esz(ex->out_dt);
+        std::vector<BuiltPlan> plans(ex->plans.size());
+        for (size_t b = 0; b < ex->plans.size(); ++b) {
+            std::vector<Dest> d = ex->dests[b];
+            for (Dest& t : d)
+                for (void*& p : t.ptrs) {
+                    const char* q = static_cast<const char*>(p);
+                    int hit = -1;
+                    for (int i = 0; i < n_regions && hit < 0; ++i) {
+                        const char* base = static_cast<const char*>(region_dev[i]);
+                        if (region_bytes[i] > 0 && q >= base && q + t.numel * osz <= base + region_bytes[i]) hit = i;
+                    }
+                    if (hit < 0) return set_error(DPRED_E_INVAL, "bucket %zu writes outside every output region", b);
+                    p = hdev[hit] + (q - static_cast<const char*>(region_dev[hit]));
+                }
+            build_plan(ex->world, ex->in_dt, static_cast<const char*>(gdev) + ex->start[b] * esz(ex->in_dt), host_ld,
+                       ex->out_dt, ex->pre_div, d, plans[b]);
+            plans[b].ldg_only = true;
+        }
+        ex->mapped = std::move(plans);
+        ex->mapped_key = std::move(key);
+    }
+    for (size_t b = 0; b < ex->mapped.size(); ++b) {
+        if (probes) {
+            probes[b] = ex->probes[b];
+            probes[b].flush_index = ex->flushes;
+        }
+        ex->flushes += 1;
+        const int rc = launch_plan(ex->mapped[b], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream));
+        if (rc) return rc;
+    }
+    return DPRED_OK;
 }
 
 }  // extern "C"

@@ -562,11 +562,13 @@ int64_t persistent_grid(K kernel, int64_t units) {
 }
 
 // One launch of the LDG kernel (any W) or, for W in {2, 4, 8, 16} when the
-// TMA path is selected, of the TMA-staged kernel (one CTA per SM).
+// TMA path is selected, of the TMA-staged kernel (one CTA per SM).  Plans that
+// touch host memory always take the LDG kernel: its plain loads and stores
+// reach pinned host memory over the host link, and no bulk copy is issued there.
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
-cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, cudaStream_t s) {
+cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_only, cudaStream_t s) {
     if constexpr (W_T > 0) {
-        if (flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
+        if (!ldg_only && flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
             auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
             constexpr size_t smem = tma_smem_bytes<W_T>();
             static bool attr[64] = {};
@@ -599,7 +601,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         for (int i = 0; i < h.n_tasks; ++i) a.tasks[i] = L.tasks[i];
         for (int i = 0; i < L.n_dst; ++i) a.dst[i] = L.dst[i];
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, s);
     } else {
         size_t tb = sizeof(TaskDesc) * (size_t)h.n_tasks, db = sizeof(void*) * (size_t)L.n_dst;
         size_t need = tb + ((db + 15) & ~(size_t)15);
@@ -616,7 +618,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         a.tasks = reinterpret_cast<const TaskDesc*>(ws);
         a.dst = reinterpret_cast<void* const*>(ws + tb);
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, s);
     }
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
 }
