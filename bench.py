@@ -671,6 +671,25 @@ def rows(peak):
         out[f"torch_zero_fill_{N}GiB"] = entry(ms, N * Mel * 2, workload="write-only reference (torch zero_)")
         del wr
         del ag, rs
+    # HBM write ceiling, measured by the same TMA AllGather with N=64: 16 GiB of
+    # stores against 256 MiB of loads (98.5% writes).  The N=8 and N=4 rows
+    # are then compared with the time that ceiling plus the copy peak for the
+    # loads predicts.
+    N, S = 64, 1 << 21
+    x = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
+    datagen.fill_device(x.data_ptr(), N, S, S, BF16, UNIFORM, 5, 0, 1, 0, 1.0, s)
+    ag = torch.empty((N, N * S), dtype=torch.bfloat16, device="cuda")
+    ms = timed(lambda: zc.allgather(x, ag, 0), 5)
+    w64 = N * N * S * 2
+    write_gbs = w64 / (ms * 1e-3) / 1e9
+    out["allgather_N64_write_ceiling"] = entry(ms, w64 + N * S * 2, workload="N=64, 4 MiB shards: 16 GiB written")
+    out["allgather_N64_write_ceiling"]["write_GBps"] = round(write_gbs, 1)
+    del x, ag
+    for N in (8, 4):
+        for name in ("canonical", "ring"):
+            r = out[f"allgather_{name}_N{N}"]
+            model_ms = (N * Mel * 2 / (write_gbs * 1e9) + Mel * 2 / (peak * 1e9)) * 1e3
+            r["frac_of_write_model"] = round(model_ms / r["ms"], 4)
     out["allgather_schedules_N8"] = schedule_fit(8, Mel)
     torch.cuda.empty_cache()
     return out

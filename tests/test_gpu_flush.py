@@ -218,3 +218,47 @@ def test_402m_w8_full_size_sampled():
     # probe totals
     assert sum(p.owner_elems for p in probes) == 295_798_784
     assert sum(p.reduced_elems for p in probes) == tree.total
+
+
+def test_indices_beyond_int32():
+    """A task longer than 2^31 elements and a task that starts past element
+    2^31 of its row: every 64-bit index path (unit search, vector and scalar
+    offsets, destinations) is exercised.  W=2 bf16, 8.6 GB of gradients;
+    sampled elements against the oracle, the ends of every destination and
+    the canaries around them checked exactly."""
+    world, seed, sigma = 2, 41, 1e-2
+    big = (1 << 31) + 11                      # numel above INT32_MAX, starts unaligned (head of 3)
+    off1 = (1 << 31) + 100                    # second task starts past 2^31
+    n1 = 3 * (1 << 20) - 77                   # ragged tail
+    ld = off1 + n1 + 29
+    grads = device_matrix(world, ld, BF16, NORMAL, seed, sigma=sigma)
+    tasks = np.zeros(2, dtype=zc.TASK_DTYPE)
+    tasks[0] = (0, 0, 5, big)
+    tasks[1] = (1, 0, off1, n1)
+    owner = np.array([1, -1], np.int32)       # param 0 reduced to rank 1, param 1 to both ranks
+    g = 8
+    b0 = torch.full((big + 2 * g,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    b1 = [torch.full((n1 + 2 * g,), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    table = zc.DstTable(world, 2, [0, b1[0][g:].data_ptr(), b0[g:].data_ptr(), b1[1][g:].data_ptr()])
+    pr = zc.flush_bucket(grads, tasks, owner, table, BF16, True, True, probe=True)
+    torch.cuda.synchronize()
+    assert zc.device_status() == 0
+    assert pr.reduced_elems == big + n1 and pr.owner_elems == big
+    rng = np.random.default_rng(7)
+
+    def check(buf, off, n, picks):
+        ks = np.array(sorted(set(int(k) for k in picks if 0 <= k < n)), np.int64)
+        cols = off + ks
+        x = np.stack([datagen.sample_host(np.full(len(cols), r), cols, BF16, NORMAL, seed, sigma) for r in range(world)])
+        want = oracle.reduce_rows(x, pre_div=True)
+        got = to_bits(buf[g + torch.from_numpy(ks).cuda()])
+        assert np.array_equal(got, np_bits(want))
+        assert torch.isnan(buf[:g].float()).all() and torch.isnan(buf[g + n:].float()).all()
+
+    edge = [0, 1, 2, 3, 4, 5, 6, 7, 8]
+    near = [(1 << 31) - 5 - d for d in range(-12, 12)]       # task-relative positions around row element 2^31
+    check(b0, 5, big, edge + near + [big - 1 - d for d in range(16)] + list(rng.integers(0, big, 400)))
+    for r in range(world):
+        check(b1[r], off1, n1, edge + [n1 - 1 - d for d in range(16)] + list(rng.integers(0, n1, 200)))
+    # no element of the long destination was left unwritten
+    assert not torch.isnan(b0[g:g + big].float()).any()
