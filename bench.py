@@ -492,13 +492,17 @@ def cpu_baseline_all_cores(buckets, tree, seconds=1.5):
 
 
 def flush_path_ab(ex, grads, step_bytes, peak):
-    """The same flush step with each kernel family (LDG streaming vs TMA staging)."""
+    """The same flush step with each kernel family (LDG streaming vs TMA
+    staging), and with the launch overlap between buckets turned off."""
     import zero_collectives_gb300 as zc
     out = {}
     prev = zc.set_flush_path(zc.PATH_LDG)
-    for name, path in (("ldg", zc.PATH_LDG), ("tma", zc.PATH_TMA)):
+    for name, path, overlap in (("ldg", zc.PATH_LDG, True), ("ldg_no_overlap", zc.PATH_LDG, False),
+                                ("tma", zc.PATH_TMA, True)):
         zc.set_flush_path(path)
+        was = ex.set_overlap(overlap)
         ms = timed(lambda: ex.flush_all(grads), 20, warm=3)
+        ex.set_overlap(was)
         gbs = step_bytes / (ms * 1e-3) / 1e9
         out[name] = {"ms_per_step": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4)}
     zc.set_flush_path(prev)

@@ -281,6 +281,23 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
                           void* const* dst, void* workspace, size_t workspace_bytes, dpred_executor** out);
 int dpred_executor_flush(dpred_executor* ex, int32_t bucket, dpred_probe* probe, void* stream);
 int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stream);
+/*
+ * Launch overlap (no counterpart in the pages).  When no two buckets of the
+ * executor can touch the same byte (disjoint column ranges, no two
+ * destination ranges overlapping, no destination inside the gradient array;
+ * checked once at creation, and for the mapped step whenever its host
+ * pointers change), dpred_executor_flush_all and _flush_all_mapped launch
+ * every flush after the first with programmatic stream serialisation: it
+ * starts on the SMs that the previous flush's last wave leaves idle, and it
+ * still completes after the previous flush, so work queued later on the
+ * stream sees every bucket done.  The first flush of a call never overlaps
+ * the caller's earlier work.  on = 0 turns it off; on by default.  Returns
+ * the previous setting (0/1), or DPRED_E_INVAL for a null executor.
+ */
+int dpred_executor_set_overlap(dpred_executor* ex, int32_t on);
+/* 1 when the executor's device buckets passed that check, 0 when not,
+ * DPRED_E_INVAL for a null executor.  Host only. */
+int dpred_executor_overlap_eligible(const dpred_executor* ex);
 int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
                                        void* const* region_dev, void* const* region_host, const int64_t* region_bytes,
                                        dpred_probe* probes, void* stream);

@@ -271,3 +271,34 @@ def test_flush_path_and_pipeline_argument_errors(L):
                                                 None) == -1
     assert L.dpred_executor_flush(h, 3, None, None) == -1                      # bucket out of range
     assert L.dpred_executor_destroy(h) == 0
+
+
+def test_executor_overlap_eligibility(L):
+    """Consecutive flushes may overlap only when no two buckets can touch the
+    same byte: disjoint columns, disjoint destinations, no destination inside
+    the gradient array.  Host-only check at creation."""
+    world, grads, ld = 2, 0x10000, 256          # gradient array [0x10000, 0x10400) in bf16
+    owner = np.array([0, 1], np.int32)
+    tasks = _tasks([(0, 0, 64), (1, 0, 64)])
+    counts = np.array([1, 1], np.int32)
+
+    def eligible(start1, dst_b1):
+        starts = np.array([0, start1], np.int64)
+        dst = (ctypes.c_void_p * 4)(0x100000, None, None, dst_b1)   # bucket 0: rank 0; bucket 1: rank 1
+        h = ctypes.c_void_p()
+        assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, grads, ld, 2, starts.ctypes.data,
+                                       counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == 0
+        e = L.dpred_executor_overlap_eligible(h)
+        if e == 1:
+            assert L.dpred_executor_set_overlap(h, 0) == 1             # on by default
+            assert L.dpred_executor_set_overlap(h, 1) == 0
+        assert L.dpred_executor_destroy(h) == 0
+        return e
+
+    assert eligible(64, 0x200000) == 1
+    assert eligible(32, 0x200000) == 0              # bucket columns [0, 64) and [32, 96) overlap
+    assert eligible(64, grads + 512) == 0           # a destination inside the gradient array
+    assert eligible(64, 0x100000 + 64) == 0         # bucket 1 writes into bucket 0's destination
+    assert eligible(64, 0x100000 + 128) == 1        # adjacent, not overlapping
+    assert L.dpred_executor_overlap_eligible(None) == -1
+    assert L.dpred_executor_set_overlap(None, 1) == -1

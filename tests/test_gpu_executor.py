@@ -166,3 +166,30 @@ def test_mapped_step_rejects_pageable_host_memory():
     assert e.value.code == -3                     # DPRED_E_SIZE
     assert zc.host_mapped_pointer(pinned) != 0
     ex.close()
+
+
+@pytest.mark.parametrize("world", [2, 8])
+def test_overlapped_launches_equal_serial_and_keep_stream_order(world):
+    """Consecutive bucket flushes launched with programmatic stream
+    serialisation give the serial result bit for bit, and work queued on the
+    stream right after the step (a copy of every buffer) sees every bucket."""
+    tree = workloads.straddle_tree(world, 150000 * world + 13, world - 1, pieces=6)
+    layout, grads, ex = _setup(world, tree, capacity=tree.total // 6)
+    assert len(layout.buckets) >= 5
+    ex._bind(grads)
+    assert zc.lib().dpred_executor_overlap_eligible(ex._native) == 1
+    ex.set_overlap(False)
+    ex.flush_all(grads)
+    torch.cuda.synchronize()
+    serial = [b.clone() for b in ex.grad.buf]
+    ex.set_overlap(True)
+    for _ in range(3):
+        for b in ex.grad.buf:
+            b.fill_(float("nan"))
+        ex.flush_all(grads)
+        after = [b.clone() for b in ex.grad.buf]   # same stream, queued right behind the last flush
+        torch.cuda.synchronize()
+        for r in range(world):
+            assert torch.equal(after[r].view(torch.int16), serial[r].view(torch.int16))
+    assert zc.device_status() == 0
+    ex.close()

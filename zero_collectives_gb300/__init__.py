@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
                                             ctypes.c_size_t, vp]
         L.dpred_executor_flush.argtypes = [vp, i32, vp, vp]
         L.dpred_executor_flush_all.argtypes = [vp, vp, vp]
+        L.dpred_executor_set_overlap.argtypes = [vp, i32]
+        L.dpred_executor_overlap_eligible.argtypes = [vp]
         L.dpred_executor_flush_all_from_host.argtypes = [vp, vp, i64, i32, vp, vp, vp, vp, vp]
         L.dpred_executor_destroy.argtypes = [vp]
         L.dpred_flush_bucket_noalloc.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp,
@@ -579,6 +581,7 @@ class Zero1Executor:
         self.probe_log = probe_log
         ws = max((flush_workspace_bytes(world, len(t)) for _, t in self.buckets), default=0)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda") if ws else None
+        self.overlap = True
         self._native = None
         self._bound = None
 
@@ -610,6 +613,16 @@ class Zero1Executor:
                                            tasks.ctypes.data, dst, ws_ptr, ws_bytes, ctypes.byref(handle)))
         self._native = handle
         self._bound = key
+        lib().dpred_executor_set_overlap(self._native, int(self.overlap))
+
+    def set_overlap(self, on: bool) -> bool:
+        """Let consecutive bucket flushes of a step overlap on the GPU (the
+        default; used only when the buckets share no byte).  Returns the
+        previous setting."""
+        prev, self.overlap = self.overlap, bool(on)
+        if self._native is not None:
+            lib().dpred_executor_set_overlap(self._native, int(self.overlap))
+        return prev
 
     def close(self):
         if self._native is not None and _lib is not None:

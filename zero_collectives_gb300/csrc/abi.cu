@@ -84,7 +84,7 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     out.out_dt = out_dt;
 }
 
-int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s) {
+int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl) {
     if (p.tasks.empty()) return DPRED_OK;
     FlushLaunch L{};
     L.h = p.h;
@@ -98,6 +98,7 @@ int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cud
     L.workspace_bytes = workspace_bytes;
     L.realign = p.realign;
     L.ldg_only = p.ldg_only;
+    L.pdl = pdl;
     return p.in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
 }
 

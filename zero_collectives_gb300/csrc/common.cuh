@@ -129,6 +129,7 @@ struct FlushLaunch {
     size_t workspace_bytes;
     bool realign;            // some task takes the realigned vector path
     bool ldg_only;           // register streaming only: an operand lives in host memory
+    bool pdl;                // may overlap the previous launch on the stream (disjoint buckets only)
 };
 
 // Vectors each thread keeps in flight per replica row: small world sizes take
@@ -163,7 +164,9 @@ struct BuiltPlan {
 
 void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt, int pre_div,
                 const std::vector<Dest>& tasks, BuiltPlan& out);
-int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s);
+// pdl: launch with programmatic stream serialisation (the caller guarantees
+// that this flush shares no byte with the previous launch on the stream).
+int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl = false);
 
 int launch_flush_bf16_in(const FlushLaunch& L, cudaStream_t s);
 int launch_flush_f32_in(const FlushLaunch& L, cudaStream_t s);

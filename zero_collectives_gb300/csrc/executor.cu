@@ -36,6 +36,10 @@ struct dpred_executor {
     // plans of the mapped host step, rebuilt when its host pointers change
     std::vector<dpred::BuiltPlan> mapped;
     std::vector<const void*> mapped_key;
+    // launch overlap: bucket b+1's flush may start while bucket b's drains
+    bool overlap_ok = false;         // the device buckets share no byte
+    bool mapped_overlap_ok = false;  // the mapped plans share no byte
+    bool overlap_on = true;          // dpred_executor_set_overlap
     void* workspace;
     size_t workspace_bytes;
     int64_t flushes = 0;
@@ -68,6 +72,47 @@ int setup_pipeline(dpred_executor* ex) {
     if (e != cudaSuccess) return dpred::cuda_error(e, "executor stream/event creation");
     ex->pipeline = true;
     return DPRED_OK;
+}
+
+// True when no two flushes of the step can touch the same byte: the buckets'
+// column ranges are disjoint, no two destination ranges overlap, and no
+// destination lies inside the gradient array [grads, grads + grads_bytes).
+// Only then may consecutive flushes overlap on the GPU.
+bool buckets_independent(const std::vector<int64_t>& start, const std::vector<int64_t>& size,
+                         const std::vector<std::vector<dpred::Dest>>& dests, int osz, const void* grads,
+                         int64_t grads_bytes) {
+    std::vector<std::pair<int64_t, int64_t>> cols;
+    for (size_t b = 0; b < start.size(); ++b)
+        if (size[b] > 0) cols.emplace_back(start[b], start[b] + size[b]);
+    std::sort(cols.begin(), cols.end());
+    for (size_t i = 1; i < cols.size(); ++i)
+        if (cols[i].first < cols[i - 1].second) return false;
+    const uintptr_t g0 = reinterpret_cast<uintptr_t>(grads), g1 = g0 + (uintptr_t)grads_bytes;
+    std::vector<std::pair<uintptr_t, uintptr_t>> r;
+    for (const auto& bd : dests)
+        for (const dpred::Dest& t : bd)
+            if (t.numel > 0)
+                for (void* p : t.ptrs) {
+                    const uintptr_t a = reinterpret_cast<uintptr_t>(p), e = a + (uintptr_t)(t.numel * osz);
+                    if (a < g1 && e > g0) return false;
+                    r.emplace_back(a, e);
+                }
+    std::sort(r.begin(), r.end());
+    uintptr_t end = 0;
+    for (const auto& x : r) {
+        if (x.first < end) return false;
+        end = std::max(end, x.second);
+    }
+    return true;
+}
+
+int flush_one(dpred_executor* ex, int b, dpred_probe* probe, void* stream, bool pdl) {
+    if (probe) {
+        *probe = ex->probes[b];
+        probe->flush_index = ex->flushes;
+    }
+    ex->flushes += 1;
+    return dpred::launch_plan(ex->plans[b], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream), pdl);
 }
 
 void release(dpred_executor* ex) {
@@ -189,6 +234,8 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
         t0 += nt;
         d0 += (int64_t)world * nt;
     }
+    ex->overlap_ok = buckets_independent(ex->start, ex->size, ex->dests, esz(out_dtype), grads,
+                                         (int64_t)world * ld * esz(in_dtype));
     *out = ex;
     return DPRED_OK;
 }
@@ -205,21 +252,30 @@ int dpred_executor_flush(dpred_executor* ex, int32_t bucket, dpred_probe* probe,
     if (!ex) return set_error(DPRED_E_INVAL, "null executor");
     if (bucket < 0 || bucket >= (int)ex->plans.size())
         return set_error(DPRED_E_INVAL, "bucket %d outside 0..%d", bucket, (int)ex->plans.size() - 1);
-    if (probe) {
-        *probe = ex->probes[bucket];
-        probe->flush_index = ex->flushes;
-    }
-    ex->flushes += 1;
-    return launch_plan(ex->plans[bucket], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream));
+    return flush_one(ex, bucket, probe, stream, false);
 }
 
 int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stream) {
     if (!ex) return dpred::set_error(DPRED_E_INVAL, "null executor");
+    const bool pdl = ex->overlap_ok && ex->overlap_on;
     for (int b = 0; b < (int)ex->plans.size(); ++b) {
-        int rc = dpred_executor_flush(ex, b, probes ? probes + b : nullptr, stream);
+        // the first flush follows the caller's own work: never overlapped
+        int rc = flush_one(ex, b, probes ? probes + b : nullptr, stream, pdl && b > 0);
         if (rc) return rc;
     }
     return DPRED_OK;
+}
+
+int dpred_executor_overlap_eligible(const dpred_executor* ex) {
+    if (!ex) return dpred::set_error(DPRED_E_INVAL, "null executor");
+    return ex->overlap_ok ? 1 : 0;
+}
+
+int dpred_executor_set_overlap(dpred_executor* ex, int32_t on) {
+    if (!ex) return dpred::set_error(DPRED_E_INVAL, "null executor");
+    const int prev = ex->overlap_on ? 1 : 0;
+    ex->overlap_on = on != 0;
+    return prev;
 }
 
 int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grads, int64_t host_ld, int32_t n_regions,
@@ -322,6 +378,7 @@ int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, 
         }
         const int osz = esz(ex->out_dt);
         std::vector<BuiltPlan> plans(ex->plans.size());
+        std::vector<std::vector<Dest>> mapped_dests;
         for (size_t b = 0; b < ex->plans.size(); ++b) {
             std::vector<Dest> d = ex->dests[b];
             for (Dest& t : d)
@@ -338,7 +395,10 @@ int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, 
             build_plan(ex->world, ex->in_dt, static_cast<const char*>(gdev) + ex->start[b] * esz(ex->in_dt), host_ld,
                        ex->out_dt, ex->pre_div, d, plans[b]);
             plans[b].ldg_only = true;
+            mapped_dests.push_back(std::move(d));
         }
+        ex->mapped_overlap_ok = buckets_independent(ex->start, ex->size, mapped_dests, osz, gdev,
+                                                    (int64_t)ex->world * host_ld * esz(ex->in_dt));
         ex->mapped = std::move(plans);
         ex->mapped_key = std::move(key);
     }
@@ -348,7 +408,9 @@ int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, 
             probes[b].flush_index = ex->flushes;
         }
         ex->flushes += 1;
-        const int rc = launch_plan(ex->mapped[b], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream));
+        const bool pdl = ex->mapped_overlap_ok && ex->overlap_on && b > 0;
+        const int rc = launch_plan(ex->mapped[b], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream),
+                                   pdl);
         if (rc) return rc;
     }
     return DPRED_OK;

@@ -364,8 +364,17 @@ __device__ __forceinline__ int find_task(const Args& a, int64_t u) {
 // RA: the plan holds realigned tasks (destinations shifted against the
 // source).  That path is compiled into its own kernel so that the common
 // kernel keeps its register budget.
+//
+// Programmatic dependent launch: every CTA lets the next launch on the stream
+// start as soon as it is running, and waits for the previous launch's grid
+// to complete before it exits.  A flush launched with programmatic stream
+// serialisation (only ever one whose bucket shares no byte with the previous
+// one) therefore fills the SMs that the previous flush's last wave leaves
+// idle, and still completes after it, so the stream's order of completion is
+// unchanged.  Launched without the attribute, both instructions do nothing.
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args, bool RA>
 __global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_constant__ Args a) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const FlushHeader& h = a.h;
     for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
         const TaskDesc T = plan_task(a, find_task(a, u));
@@ -377,6 +386,7 @@ __global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_const
         else
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE, RA>(a, T, local);
     }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -565,8 +575,29 @@ int64_t persistent_grid(K kernel, int64_t units) {
 // TMA path is selected, of the TMA-staged kernel (one CTA per SM).  Plans that
 // touch host memory always take the LDG kernel: its plain loads and stores
 // reach pinned host memory over the host link, and no bulk copy is issued there.
+// Launch of the LDG kernel, with programmatic stream serialisation when pdl.
+template <typename K, typename Args>
+cudaError_t launch_ldg(K k, const Args& a, int64_t units, bool pdl, cudaStream_t s) {
+    const unsigned grid = (unsigned)persistent_grid(k, units);
+    if (!pdl) {
+        k<<<grid, kFlushThreads, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kFlushThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, a);
+}
+
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
-cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_only, cudaStream_t s) {
+cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_only, bool pdl, cudaStream_t s) {
     if constexpr (W_T > 0) {
         if (!ldg_only && flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
             auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
@@ -580,15 +611,9 @@ cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_o
         }
     }
     if constexpr (std::is_same<Tin, Tout>::value) {
-        if (realign) {
-            auto k = flush_kernel<W_T, BATCH, Tin, Tout, Args, true>;
-            k<<<(unsigned)persistent_grid(k, units), kFlushThreads, 0, s>>>(a);
-            return cudaGetLastError();
-        }
+        if (realign) return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, pdl, s);
     }
-    auto k = flush_kernel<W_T, BATCH, Tin, Tout, Args, false>;
-    k<<<(unsigned)persistent_grid(k, units), kFlushThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, pdl, s);
 }
 
 template <int W_T, int BATCH, typename Tin, typename Tout>
@@ -601,7 +626,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         for (int i = 0; i < h.n_tasks; ++i) a.tasks[i] = L.tasks[i];
         for (int i = 0; i < L.n_dst; ++i) a.dst[i] = L.dst[i];
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, L.pdl, s);
     } else {
         size_t tb = sizeof(TaskDesc) * (size_t)h.n_tasks, db = sizeof(void*) * (size_t)L.n_dst;
         size_t need = tb + ((db + 15) & ~(size_t)15);
@@ -618,7 +643,8 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         a.tasks = reinterpret_cast<const TaskDesc*>(ws);
         a.dst = reinterpret_cast<void* const*>(ws + tb);
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, s);
+        // the plan upload sits between this launch and the previous one: no overlap
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, false, s);
     }
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
 }
