@@ -560,6 +560,21 @@ def rows(peak):
         writes = sum(int(tree.numel[p]) * (1 if om.owner[p] >= 0 else WORLD) for p in range(tree.n_params))
         out[name] = entry(ms, WORLD * n * 2 + writes * 2, workload="402.8M W=8 bf16, 7 buckets, in place")
 
+    # The same model cut into small buckets (at most 4,194,304 elements, 8 MiB
+    # per replica row): about a hundred launches per step, where the overlap of
+    # consecutive flushes matters most.
+    small = workloads.arrival_layout(tree, capacity=1 << 22)
+    ex_s = zc.Zero1Executor(WORLD, tree.numel, small.row_offset, [(b.start, b.tasks) for b in small.buckets],
+                            torch.bfloat16)
+    sb = flush_bytes(WORLD, small.buckets, ex_s.omap, owner_mode_writes(ex_s.omap))
+    for overlap, name in ((True, "flush_step_small_buckets"), (False, "flush_step_small_buckets_no_overlap")):
+        ex_s.set_overlap(overlap)
+        ms = timed(lambda: ex_s.flush_all(g), 20, warm=3)
+        out[name] = entry(ms, sb, workload=f"402.8M W=8 bf16, {len(small.buckets)} buckets of <= 4,194,304 elements",
+                          launches=len(small.buckets))
+    ex_s.close()
+    del ex_s
+
     # Partitioned flush (every rank gets exactly its partition slice) over the
     # 7 arrival-order buckets, and over the whole model as one bucket against
     # the two-pass relayout + ReduceScatter that ncclReduceScatter would need.
