@@ -52,6 +52,8 @@ extern "C" {
 #define DPRED_E_MISMATCH (-4) /* checked mode: destinations disagree with the owner map */
 #define DPRED_E_CUDA (-5)     /* a CUDA runtime call failed */
 #define DPRED_E_TIMEOUT (-6)  /* a device-side bounded wait gave up (reported by dpred_device_status) */
+#define DPRED_E_BOUNDS (-7)   /* checked build: a kernel access failed its bounds test and was skipped
+                                 (reported by dpred_device_status) */
 
 /* element types */
 #define DPRED_BF16 0
@@ -92,6 +94,15 @@ typedef struct {
 
 const char* dpred_last_error(void);
 const char* dpred_version(void);
+/* 1 in the checked build (compiled with -DDPRED_CHECKED=1, loaded when the
+ * environment sets DPRED_CHECKED=1): every global load and store of the flush
+ * kernels (flush, ReduceScatter, the executor's steps; both kernel families)
+ * is first tested against the task it belongs to -- source vector inside the
+ * task's aligned body and inside the row, destination element range inside
+ * the task -- and a failed test records DPRED_E_BOUNDS in the device error
+ * word and skips the access.  0 in the default build, where the tests compile
+ * away.  No counterpart in the pages. */
+int dpred_checked_build(void);
 
 /*
  * Owner map.  [DS] "Design points" ("Owner map costs nothing to build",
@@ -497,6 +508,15 @@ int dpred_host_mapped_pointer(const void* host, void** dev);
  * context stays usable.  Asynchronous on `stream`.
  */
 int dpred_selftest_wait_timeout(int64_t budget_cycles, void* stream);
+
+/*
+ * Self-test of the bounds-test path (no counterpart in the pages): one thread
+ * runs the flush kernels' access test on index 16 of a 16-element range.  The
+ * checked build (dpred_checked_build() == 1) records DPRED_E_BOUNDS in the
+ * device error word; the default build records nothing.  No memory is
+ * accessed in either build.  Asynchronous on `stream`.
+ */
+int dpred_selftest_bounds(void* stream);
 
 #ifdef __cplusplus
 }

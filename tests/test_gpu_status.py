@@ -24,3 +24,14 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 def test_selftest_rejects_bad_budget():
     with pytest.raises(zc.DpredError):
         zc.selftest_wait_timeout(-1)
+
+
+def test_bounds_selftest_matches_the_build():
+    """The access test on an out-of-range index records DPRED_E_BOUNDS in the
+    checked build and nothing in the default build; nothing is accessed."""
+    zc.device_status(clear=True)
+    zc.selftest_bounds()
+    torch.cuda.synchronize()
+    want = -7 if zc.checked_build() else 0
+    assert zc.device_status(clear=True) == want
+    assert zc.device_status() == 0

@@ -15,7 +15,11 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libdpred.so")
+# DPRED_CHECKED=1 in the environment loads the checked build instead (every
+# flush-kernel access bounds-tested on the device; build it with
+# zero_collectives_gb300.build.build(checked=True)).
+CHECKED = os.environ.get("DPRED_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(_HERE, "libdpred_checked.so" if CHECKED else "libdpred.so")
 
 BF16, F32 = 0, 1
 MAX_WORLD = 64
@@ -25,7 +29,7 @@ DTYPE_NAMES = {BF16: "BFloat16", F32: "Float"}  # names the probe line prints
 TASK_DTYPE = np.dtype([("param_id", "<i4"), ("pad", "<i4"), ("offset", "<i8"), ("numel", "<i8")])
 
 E_CODES = {-1: "DPRED_E_INVAL", -2: "DPRED_E_ALIGN", -3: "DPRED_E_SIZE", -4: "DPRED_E_MISMATCH",
-           -5: "DPRED_E_CUDA", -6: "DPRED_E_TIMEOUT"}
+           -5: "DPRED_E_CUDA", -6: "DPRED_E_TIMEOUT", -7: "DPRED_E_BOUNDS"}
 
 
 class DpredError(RuntimeError):
@@ -53,8 +57,8 @@ def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
-                              "(there is no fallback path)")
+            how = "build.build(checked=True)" if CHECKED else "__graft_entry__.build()"
+            raise ImportError(f"{LIB_PATH} is missing: build it with {how} (there is no fallback path)")
         L = ctypes.CDLL(LIB_PATH)
         i32, i64, vp, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_float
         L.dpred_last_error.restype = ctypes.c_char_p
@@ -95,6 +99,7 @@ def lib() -> ctypes.CDLL:
         L.dpred_device_status.argtypes = [vp, i32]
         L.dpred_set_flush_path.argtypes = [i32]
         L.dpred_selftest_wait_timeout.argtypes = [i64, vp]
+        L.dpred_selftest_bounds.argtypes = [vp]
         L.dpred_host_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
         L.dpred_executor_flush_all_mapped.argtypes = L.dpred_executor_flush_all_from_host.argtypes
         _lib = L
@@ -477,6 +482,15 @@ def allgather_schedule_step(schedule: int, bufs, step: int, stream=None):
     N = bufs.shape[0]
     _check(lib().dpred_allgather_schedule_step(schedule, N, bufs.shape[1] // N, _dtype_code(bufs), bufs.data_ptr(),
                                                int(step), _stream(stream)))
+
+
+def checked_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(lib().dpred_checked_build())
+
+
+def selftest_bounds(stream=None) -> None:
+    _check(lib().dpred_selftest_bounds(_stream(stream)))
 
 
 def device_status(clear: bool = False) -> int:

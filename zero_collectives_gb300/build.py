@@ -16,6 +16,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdpred.so")
 OBJDIR = os.path.join(HERE, "_build")
+# The checked build (device-side bounds tests on every flush-kernel access,
+# failures recorded as DPRED_E_BOUNDS) is a separate library, built on demand.
+LIB_CHECKED = os.path.join(HERE, "libdpred_checked.so")
+OBJDIR_CHECKED = os.path.join(HERE, "_build_checked")
 SOURCES = ["abi.cu", "flush_bf16.cu", "flush_f32.cu", "accumulate.cu", "allgather.cu", "noalloc.cu", "selftest.cu", "relayout.cu", "schedule.cu", "owner_map.cu", "executor.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", *ARCH, "-lineinfo", "-std=c++17", "--fmad=false", "-Xcompiler", "-fPIC", "-I", INCLUDE,
@@ -27,15 +31,15 @@ def _deps() -> list[str]:
     return [f for f in files if f.endswith((".cu", ".cuh", ".h"))]
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB):
+def stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(f) > t for f in _deps() + [os.path.abspath(__file__)])
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(OBJDIR, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra: list[str], objdir: str = OBJDIR) -> str:
+    obj = os.path.join(objdir, os.path.splitext(src)[0] + ".o")
     cmd = ["nvcc", *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -43,19 +47,22 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not stale():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    lib, objdir = (LIB_CHECKED, OBJDIR_CHECKED) if checked else (LIB, OBJDIR)
+    if not force and not stale(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if checked:
+        extra.append("-DDPRED_CHECKED=1")
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, objdir), SOURCES))
+    tmp = lib + ".tmp"
     r = subprocess.run(["nvcc", *ARCH, "-shared", *objs, "-o", tmp], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -170,6 +170,14 @@ const char* dpred_last_error(void) { return t_last_error.c_str(); }
 
 const char* dpred_version(void) { return "dpred 0.1 (sm_103a)"; }
 
+int dpred_checked_build(void) {
+#if defined(DPRED_CHECKED) && DPRED_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 int dpred_build_owner_map(int32_t world, int32_t rank, const dpred_group* groups, int32_t n_groups,
                           int32_t reduce_to_owner, int32_t* owner, int32_t* holder_lo, int32_t* holder_hi,
                           int32_t* n_owned, int32_t* n_total) {

@@ -191,4 +191,31 @@ int* device_error_word();  // device address of the error word (current device)
 enum FlushPath : int { PATH_AUTO = 0, PATH_LDG = 1, PATH_TMA = 2 };
 int flush_path();
 
+#ifdef __CUDACC__
+__device__ __forceinline__ void record_device_error(int* err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// Checked builds (-DDPRED_CHECKED=1) test every global access of the flush
+// kernels against the task it belongs to before making it.  A failed test
+// records DPRED_E_BOUNDS in the device error word, and the access is skipped:
+// a load reads zeros, a store does not happen.  In the default build every
+// test is the constant true and compiles away.
+#ifndef DPRED_CHECKED
+#define DPRED_CHECKED 0
+#endif
+__device__ __forceinline__ bool access_ok(bool ok, int* err) {
+#if DPRED_CHECKED
+    if (!ok) {
+        record_device_error(err, DPRED_E_BOUNDS);
+        return false;
+    }
+#else
+    (void)ok;
+    (void)err;
+#endif
+    return true;
+}
+#endif
+
 }  // namespace dpred

@@ -90,6 +90,16 @@ __device__ __forceinline__ void store_vec<float, 4>(float* p, const float (&y)[4
     __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
 }
 
+// A 16-byte streaming load that a checked build skips (reads zeros) when its
+// bounds test failed; see access_ok.
+__device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
+#if DPRED_CHECKED
+    return ok ? __ldcs(p) : make_uint4(0u, 0u, 0u, 0u);
+#else
+    return __ldcs(p);
+#endif
+}
+
 // Fold one replica's vector into the running sums (rank order is the call order).
 template <typename Tin, int MODE>
 __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q, bool first, float wf, float inv_w) {
@@ -107,6 +117,7 @@ __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q
 template <typename Tin, typename Tout, int MODE, typename Args>
 __device__ void flush_element(const Args& a, const TaskDesc& T, int64_t k) {
     const FlushHeader& h = a.h;
+    if (!access_ok(k >= 0 && k < T.numel && T.src_off + k < h.ld, h.err)) return;
     const Tin* x = static_cast<const Tin*>(h.grads) + T.src_off + k;
     float y = 0.0f;
     for (int r = 0; r < h.world; ++r) {
@@ -123,6 +134,7 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
     const FlushHeader& h = a.h;
     const int64_t stride = h.ld / VEC;  // row stride in vectors
     const uint4* base = reinterpret_cast<const uint4*>(static_cast<const Tin*>(h.grads) + T.src_off + T.head);
+    const int64_t nbody = (T.numel - T.head) / VEC;  // used by the checks only
 #pragma unroll 1
     for (int64_t vb = v0 + threadIdx.x; vb < v1; vb += (int64_t)kFlushThreads * BATCH) {
         float y[BATCH][VEC];
@@ -133,8 +145,9 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
                 const int64_t v = vb + (int64_t)b * kFlushThreads < v1 ? vb + (int64_t)b * kFlushThreads : vb;
+                const bool ok = access_ok(v >= 0 && v < nbody && T.src_off + T.head + (v + 1) * VEC <= h.ld, h.err);
 #pragma unroll
-                for (int r = 0; r < W_T; ++r) q[r][b] = __ldcs(base + r * stride + v);
+                for (int r = 0; r < W_T; ++r) q[r][b] = load_vec(base + r * stride + v, ok);
             }
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
@@ -145,6 +158,7 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
             // Any world size: rows in chunks of 8 loads in flight, folded in rank order.
             static_assert(BATCH == 1, "generic path keeps one vector per thread");
             int64_t v = vb;
+            const bool ok = access_ok(v >= 0 && v < nbody && T.src_off + T.head + (v + 1) * VEC <= h.ld, h.err);
             for (int r0 = 0; r0 < h.world; r0 += 8) {
                 // rows past the last one re-read the last row (no branch around
                 // the loads) and are not folded
@@ -152,7 +166,7 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                     const int row = r0 + r < h.world ? r0 + r : h.world - 1;
-                    q[r] = __ldcs(base + (int64_t)row * stride + v);
+                    q[r] = load_vec(base + (int64_t)row * stride + v, ok);
                 }
 #pragma unroll
                 for (int r = 0; r < 8; ++r)
@@ -162,8 +176,8 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
             int64_t v = vb + (int64_t)b * kFlushThreads;
-            if (v < v1) {
-                int64_t e = T.head + v * VEC;  // element index inside the task
+            const int64_t e = T.head + v * VEC;  // element index inside the task
+            if (v < v1 && access_ok(e >= 0 && e + VEC <= T.numel, h.err)) {
                 for (int d = 0; d < T.ndst; ++d)
                     store_vec<Tout, VEC>(static_cast<Tout*>(plan_dst(a, T.dst_begin + d)) + e, y[b]);
             }
@@ -237,17 +251,17 @@ __device__ __forceinline__ uint4 shifted_rt(int s, const uint4& P, const uint4& 
 // Reduced, packed source vector v of the task (rows in rank order).
 template <int W_T, typename T, int MODE>
 __device__ __forceinline__ uint4 reduce_packed(const uint4* base, int64_t stride, int64_t v, int world, float wf,
-                                               float inv_w) {
+                                               float inv_w, bool ok) {
     constexpr int VEC = Elem<T>::kVec;
     float y[VEC];
     if constexpr (W_T > 0) {
         uint4 q[W_T];
 #pragma unroll
-        for (int r = 0; r < W_T; ++r) q[r] = __ldcs(base + r * stride + v);
+        for (int r = 0; r < W_T; ++r) q[r] = load_vec(base + r * stride + v, ok);
 #pragma unroll
         for (int r = 0; r < W_T; ++r) fold<T, MODE>(y, q[r], r == 0, wf, inv_w);
     } else {
-        for (int r = 0; r < world; ++r) fold<T, MODE>(y, __ldcs(base + (int64_t)r * stride + v), r == 0, wf, inv_w);
+        for (int r = 0; r < world; ++r) fold<T, MODE>(y, load_vec(base + (int64_t)r * stride + v, ok), r == 0, wf, inv_w);
     }
     return pack_vec<T>(y);
 }
@@ -279,7 +293,9 @@ __device__ __forceinline__ void flush_unit_realign(const Args& a, const TaskDesc
     for (int64_t pb = v0; pb < v1; pb += kFlushThreads) {
         const int64_t v = pb + t;
         const int64_t vl = v < v1 ? v : v1 - 1;
-        const uint4 C = reduce_packed<W_T, T, MODE>(base, stride, vl, h.world, h.wf, h.inv_w);
+        const bool ok = access_ok(vl >= 0 && vl < (Tk.numel - Tk.head) / VEC &&
+                                      Tk.src_off + Tk.head + (vl + 1) * VEC <= h.ld, h.err);
+        const uint4 C = reduce_packed<W_T, T, MODE>(base, stride, vl, h.world, h.wf, h.inv_w, ok);
         uint4 P;
         P.x = __shfl_up_sync(0xffffffffu, C.x, 1);
         P.y = __shfl_up_sync(0xffffffffu, C.y, 1);
@@ -290,9 +306,9 @@ __device__ __forceinline__ void flush_unit_realign(const Args& a, const TaskDesc
         if (lane == 0) P = warp > 0 ? s_last[warp - 1] : s_carry;  // s_carry: set by the previous pass
         reducers_barrier();
         if (t == kFlushThreads - 1) s_carry = C;
-        if (v > v0 && v < v1) {
+        const int64_t e = Tk.head + v * VEC - sigma;  // destination-aligned element index
+        if (v > v0 && v < v1 && access_ok(e >= 0 && e + VEC <= Tk.numel, h.err)) {
             const uint4 out = shifted_rt<T>(sigma, P, C);
-            const int64_t e = Tk.head + v * VEC - sigma;  // destination-aligned element index
             for (int d = 0; d < Tk.ndst; ++d)
                 __stcs(reinterpret_cast<uint4*>(static_cast<T*>(plan_dst(a, Tk.dst_begin + d)) + e), out);
         }
@@ -419,10 +435,6 @@ __host__ __device__ constexpr size_t tma_smem_bytes() {
     return (size_t)tma_stages<W>() * W * kTmaRowBytes;
 }
 
-__device__ __forceinline__ void record_device_error(int* err, int code) {
-    if (err) atomicCAS(err, 0, code);
-}
-
 template <int W_T, typename Tin, typename Tout, int MODE, typename Args>
 __device__ void tma_consume(const Args& a, unsigned char* smem, uint64_t* full, uint64_t* empty, int* abort_flag) {
     constexpr int VEC = Elem<Tin>::kVec;
@@ -470,8 +482,9 @@ __device__ void tma_consume(const Args& a, unsigned char* smem, uint64_t* full, 
                     fold<Tin, MODE>(y, q, r == 0, h.wf, h.inv_w);
                 }
                 const int64_t e = T.head + (sv + ctid) * VEC;
-                for (int d = 0; d < T.ndst; ++d)
-                    store_vec<Tout, VEC>(static_cast<Tout*>(plan_dst(a, T.dst_begin + d)) + e, y);
+                if (access_ok(e >= 0 && e + VEC <= T.numel, h.err))
+                    for (int d = 0; d < T.ndst; ++d)
+                        store_vec<Tout, VEC>(static_cast<Tout*>(plan_dst(a, T.dst_begin + d)) + e, y);
             }
             __syncwarp();
             if (lane == 0) tma::mbar_arrive(&empty[stage]);
@@ -507,11 +520,17 @@ __device__ void tma_produce(const Args& a, unsigned char* smem, uint64_t* full, 
                 ok = false;
                 break;
             }
-            tma::mbar_arrive_expect_tx(&full[stage], bytes * W_T);
+            // a checked build that rejects the range completes the stage with no bytes
+            const bool in = access_ok(sv >= 0 && (sv * 16 + bytes) <= nbody * 16 &&
+                                          T.src_off + T.head + (sv * 16 + bytes) / (int64_t)sizeof(Tin) <= h.ld,
+                                      h.err);
+            tma::mbar_arrive_expect_tx(&full[stage], in ? bytes * W_T : 0u);
+            if (in) {
 #pragma unroll
-            for (int r = 0; r < W_T; ++r)
-                tma::bulk_load(smem + ((size_t)stage * W_T + r) * kTmaRowBytes, base + r * row_bytes + sv * 16, bytes,
-                               &full[stage]);
+                for (int r = 0; r < W_T; ++r)
+                    tma::bulk_load(smem + ((size_t)stage * W_T + r) * kTmaRowBytes, base + r * row_bytes + sv * 16,
+                                   bytes, &full[stage]);
+            }
             ++issued;
             if (++stage == STAGES) {
                 stage = 0;
