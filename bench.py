@@ -591,6 +591,15 @@ def rows(peak):
     ms = timed(part7, 5)
     out["flush_partitioned_step"] = entry(ms, WORLD * n * 2 + n * 2,
                                           workload="402.8M W=8 bf16, 7 buckets, each rank its partition slice")
+    # the same through the partitioned executor (one native call, overlapped launches),
+    # on the 7 buckets and on 98 small ones
+    for lay, name in ((layout, "partitioned_executor_step"), (small, "partitioned_executor_step_small_buckets")):
+        pex = zc.PartitionedExecutor(WORLD, tree.numel, lay.row_offset, [(b.start, b.tasks) for b in lay.buckets],
+                                     torch.bfloat16, parts=parts)
+        ms = timed(lambda: pex.flush_all(g), 20, warm=3)
+        out[name] = entry(ms, WORLD * n * 2 + n * 2, workload=f"402.8M W=8 bf16, {len(lay.buckets)} buckets",
+                          launches=len(lay.buckets))
+        pex.close()
     one = workloads.arrival_layout(tree, capacity=None).buckets[0]
     ms = timed(lambda: zc.flush_bucket_partitioned(g, one.tasks, flat, P, parts, zc.BF16, True, workspace=wsf), 5)
     out["flush_partitioned_one_bucket"] = entry(ms, WORLD * n * 2 + n * 2, workload="402.8M W=8 bf16 as one bucket")

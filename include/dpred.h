@@ -290,6 +290,24 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
                           const int32_t* owner, int32_t n_params, const void* grads, int64_t ld, int32_t n_buckets,
                           const int64_t* bucket_start, const int32_t* bucket_tasks, const dpred_task* tasks,
                           void* const* dst, void* workspace, size_t workspace_bytes, dpred_executor** out);
+/*
+ * The same executor over partitioned flushes (the ZeRO-2 form of rows f1/f3,
+ * see dpred_flush_bucket_partitioned): bucket b's tasks are cut at the
+ * partition boundaries of the flat space (flat_offset[param_id], partitions of
+ * part_size elements) and every piece is written into its rank's partition
+ * buffer part_dst[rank] (device, part_size elements of out_dtype; NULL =
+ * that rank's partition is not kept).  Every other call above works on it
+ * unchanged: flush, flush_all (with launch overlap), the two host-buffer
+ * steps (the regions are then the partition buffers), destroy.  The probes
+ * count as the partitioned flush's do.  Errors as in
+ * dpred_flush_bucket_partitioned and dpred_executor_create.
+ */
+int dpred_executor_create_partitioned(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div,
+                                      const void* grads, int64_t ld, int32_t n_buckets, const int64_t* bucket_start,
+                                      const int32_t* bucket_tasks, const dpred_task* tasks,
+                                      const int64_t* flat_offset, int32_t n_params, int64_t part_size,
+                                      void* const* part_dst, void* workspace, size_t workspace_bytes,
+                                      dpred_executor** out);
 int dpred_executor_flush(dpred_executor* ex, int32_t bucket, dpred_probe* probe, void* stream);
 int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stream);
 /*

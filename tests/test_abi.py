@@ -302,3 +302,30 @@ def test_executor_overlap_eligibility(L):
     assert eligible(64, 0x100000 + 128) == 1        # adjacent, not overlapping
     assert L.dpred_executor_overlap_eligible(None) == -1
     assert L.dpred_executor_set_overlap(None, 1) == -1
+
+
+def test_partitioned_executor_create_without_a_gpu(L):
+    """The partitioned executor builds its plans on the host: valid buckets
+    give an executor (eligible for launch overlap), and the partitioned
+    flush's argument errors come back unchanged."""
+    world, grads, ld = 2, 0x10000, 256
+    tasks = _tasks([(0, 0, 64), (1, 64, 64)])          # params 0, 1 in one bucket; flat offsets 0, 64
+    flat = np.array([0, 64], np.int64)
+    starts = np.array([0], np.int64)
+    counts = np.array([2], np.int32)
+    parts = (ctypes.c_void_p * 2)(0x100000, 0x200000)
+    h = ctypes.c_void_p()
+    assert L.dpred_executor_create_partitioned(world, 0, 0, 1, grads, ld, 1, starts.ctypes.data, counts.ctypes.data,
+                                               tasks.ctypes.data, flat.ctypes.data, 2, 64, parts, None, 0,
+                                               ctypes.byref(h)) == 0
+    assert L.dpred_executor_overlap_eligible(h) == 1
+    assert L.dpred_executor_destroy(h) == 0
+    assert L.dpred_executor_create_partitioned(world, 0, 0, 1, grads, ld, 1, starts.ctypes.data, counts.ctypes.data,
+                                               tasks.ctypes.data, flat.ctypes.data, 2, 32, parts, None, 0,
+                                               ctypes.byref(h)) == -3   # 128 elements do not fit 2 x 32
+    assert L.dpred_executor_create_partitioned(world, 0, 0, 1, grads, ld, 1, starts.ctypes.data, counts.ctypes.data,
+                                               tasks.ctypes.data, flat.ctypes.data, 2, 64, None, None, 0,
+                                               ctypes.byref(h)) == -1   # no partition table
+    assert L.dpred_executor_create_partitioned(world, 0, 0, 1, grads, 100, 1, starts.ctypes.data, counts.ctypes.data,
+                                               tasks.ctypes.data, flat.ctypes.data, 2, 64, parts, None, 0,
+                                               ctypes.byref(h)) == -3   # bucket wider than the row

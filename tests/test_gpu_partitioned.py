@@ -119,3 +119,55 @@ def test_402m_w8_partitioned_full_size_sampled():
         sel = rank == r
         idx = torch.from_numpy((f[sel] - r * P).astype(np.int64)).cuda()
         assert np.array_equal(to_bits(parts[r][idx]), want[sel]), f"rank {r}"
+
+
+@pytest.mark.parametrize("world", [4, 8])
+def test_partitioned_executor_matches_oracle_and_single_calls(world):
+    """The partitioned executor over several arrival-order buckets: every
+    partition equals the oracle's, bit for bit, with the launch overlap on and
+    off and through the mapped host step; probes equal the single calls'."""
+    tree = workloads.straddle_tree(world, 60000 * world + 31, world - 1, pieces=5)
+    layout = workloads.arrival_layout(tree, capacity=tree.total // 5)
+    assert len(layout.buckets) >= 4
+    flat = np.concatenate([[0], np.cumsum(tree.numel)[:-1]]).astype(np.int64)
+    grads = device_matrix(world, tree.total, BF16, NORMAL, 17, sigma=1e-2)
+    host = datagen.host_matrix(world, tree.total, BF16, NORMAL, 17, sigma=1e-2)
+    ex = zc.PartitionedExecutor(world, tree.numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets],
+                                torch.bfloat16)
+    P = ex.part_size
+    want = [np.zeros(P, np.uint16) for _ in range(world)]
+    for b in layout.buckets:
+        oracle.flush_partitioned(world, host[:, b.start:b.start + b.size].copy(), b.tasks, flat, P, want, BF16, True)
+    ex._bind(grads)
+    assert zc.lib().dpred_executor_overlap_eligible(ex._native) == 1
+    for overlap in (False, True):
+        ex.set_overlap(overlap)
+        for p in ex.parts:
+            p.fill_(float("nan"))
+        probes = ex.flush_all(grads, probe=True)
+        torch.cuda.synchronize()
+        for r in range(world):
+            used = min(P, max(0, tree.total - r * P))     # the last partition is shorter
+            got = to_bits(ex.parts[r])
+            assert np.array_equal(got[:used], want[r][:used]), f"rank {r}, overlap {overlap}"
+            assert torch.isnan(ex.parts[r][used:].float()).all()
+    ws = torch.empty(zc.flush_workspace_bytes(world, max(len(b.tasks) for b in layout.buckets) + world), dtype=torch.uint8,
+                     device="cuda")
+    scratch = [torch.empty(P, dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    for i, b in enumerate(layout.buckets):
+        pr = zc.flush_bucket_partitioned(grads[:, b.start:b.start + b.size], b.tasks, flat, P, scratch, BF16, True,
+                                         probe=True, workspace=ws)
+        q = probes[i]
+        assert (pr.tasks, pr.reduced_elems, pr.owner_elems, pr.kept_elems) == \
+            (q.tasks, q.reduced_elems, q.owner_elems, q.kept_elems)
+    # the mapped host step: gradients and partitions in pinned host memory
+    hg = torch.from_numpy(host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    outs = [torch.full((P,), float("nan"), dtype=torch.bfloat16).pin_memory() for _ in range(world)]
+    ex.flush_all_mapped(hg, outs, grads)
+    torch.cuda.synchronize()
+    for r in range(world):
+        used = min(P, max(0, tree.total - r * P))
+        assert np.array_equal(outs[r].view(torch.int16).numpy().view(np.uint16)[:used], want[r][:used]), \
+            f"mapped, rank {r}"
+    assert zc.device_status() == 0
+    ex.close()

@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
         L.dpred_executor_flush.argtypes = [vp, i32, vp, vp]
         L.dpred_executor_flush_all.argtypes = [vp, vp, vp]
         L.dpred_executor_set_overlap.argtypes = [vp, i32]
+        L.dpred_executor_create_partitioned.argtypes = [i32, i32, i32, i32, vp, i64, i32, vp, vp, vp, vp, i32, i64,
+                                                        vp, vp, ctypes.c_size_t, vp]
         L.dpred_executor_overlap_eligible.argtypes = [vp]
         L.dpred_executor_flush_all_from_host.argtypes = [vp, vp, i64, i32, vp, vp, vp, vp, vp]
         L.dpred_executor_destroy.argtypes = [vp]
@@ -611,6 +613,14 @@ class Zero1Executor:
         tasks = np.ascontiguousarray(np.concatenate([t for _, t in self.buckets]) if nb else np.zeros(0, TASK_DTYPE))
         starts = np.array([s for s, _ in self.buckets], np.int64)
         counts = np.array([len(t) for _, t in self.buckets], np.int32)
+        handle = ctypes.c_void_p()
+        ws_ptr, ws_bytes = (None, 0) if self.workspace is None else (self.workspace.data_ptr(), self.workspace.numel())
+        self._create(grads, ld, nb, starts, counts, tasks, ws_ptr, ws_bytes, handle)
+        self._native = handle
+        self._bound = key
+        lib().dpred_executor_set_overlap(self._native, int(self.overlap))
+
+    def _create(self, grads, ld, nb, starts, counts, tasks, ws_ptr, ws_bytes, handle):
         total = sum(self.world * len(t) for _, t in self.buckets)
         dst = (ctypes.c_void_p * max(total, 1))()
         pos = 0
@@ -619,15 +629,14 @@ class Zero1Executor:
             for i in range(n):
                 dst[pos + i] = tab.c[i]
             pos += n
-        handle = ctypes.c_void_p()
-        ws_ptr, ws_bytes = (None, 0) if self.workspace is None else (self.workspace.data_ptr(), self.workspace.numel())
         _check(lib().dpred_executor_create(self.world, _dtype_code(grads), self.dt_code, int(self.pre_div),
                                            int(self.reduce_to_owner), self.omap.owner.ctypes.data, len(self.omap.owner),
                                            grads.data_ptr(), ld, nb, starts.ctypes.data, counts.ctypes.data,
                                            tasks.ctypes.data, dst, ws_ptr, ws_bytes, ctypes.byref(handle)))
-        self._native = handle
-        self._bound = key
-        lib().dpred_executor_set_overlap(self._native, int(self.overlap))
+
+    def _regions(self):
+        """The device buffers the step writes into, one per rank."""
+        return self.grad.buf
 
     def set_overlap(self, on: bool) -> bool:
         """Let consecutive bucket flushes of a step overlap on the GPU (the
@@ -683,9 +692,9 @@ class Zero1Executor:
         W = self.world
         if len(host_bufs) != W:
             raise ValueError("one host buffer per rank")
-        dev = (ctypes.c_void_p * W)(*[b.data_ptr() for b in self.grad.buf])
+        dev = (ctypes.c_void_p * W)(*[b.data_ptr() for b in self._regions()])
         host = (ctypes.c_void_p * W)(*[h.data_ptr() for h in host_bufs])
-        nbytes = np.array([b.numel() * b.element_size() for b in self.grad.buf], np.int64)
+        nbytes = np.array([b.numel() * b.element_size() for b in self._regions()], np.int64)
         for h, n in zip(host_bufs, nbytes):
             if h.numel() * h.element_size() < n:
                 raise ValueError("host buffer smaller than its device buffer")
@@ -704,14 +713,62 @@ class Zero1Executor:
         W = self.world
         if len(host_bufs) != W:
             raise ValueError("one host buffer per rank")
-        for h, b in zip(host_bufs, self.grad.buf):
+        for h, b in zip(host_bufs, self._regions()):
             if h.numel() * h.element_size() < b.numel() * b.element_size():
                 raise ValueError("host buffer smaller than its device buffer")
-        dev = (ctypes.c_void_p * W)(*[b.data_ptr() for b in self.grad.buf])
+        dev = (ctypes.c_void_p * W)(*[b.data_ptr() for b in self._regions()])
         host = (ctypes.c_void_p * W)(*[h.data_ptr() for h in host_bufs])
-        nbytes = np.array([b.numel() * b.element_size() for b in self.grad.buf], np.int64)
+        nbytes = np.array([b.numel() * b.element_size() for b in self._regions()], np.int64)
         probes = self._probes(probe or self.probe_log is not None)
         hld = host_grads.stride(0) if W > 1 else host_grads.shape[1]
         _check(lib().dpred_executor_flush_all_mapped(self._native, host_grads.data_ptr(), hld, W, dev, host,
                                                      nbytes.ctypes.data, probes, _stream(stream)))
         return self._finish(probes, probe)
+
+
+class PartitionedExecutor(Zero1Executor):
+    """The executor over partitioned flushes (dpred_executor_create_partitioned):
+    every rank receives exactly its own partition of the reduced gradients,
+    the ReduceScatter form of the DeepSpeed issue's "better end state" and the
+    ZeRO-2 follow-up (real buffers with offsets).  The flat (model-order)
+    space of all parameters is cut into W partitions of P = ceil(T / W)
+    elements; ``parts[r]`` is rank r's partition buffer (P elements).  A step
+    is one native call, with the same launch overlap and host-buffer steps as
+    Zero1Executor (the host buffers then mirror ``parts``)."""
+
+    def __init__(self, world: int, numel, row_offset, buckets, dtype, pre_div: bool = True,
+                 probe_log: ProbeLog | None = None, parts=None):
+        import torch
+        self.world = world
+        self.dtype = dtype
+        self.dt_code = BF16 if dtype == torch.bfloat16 else F32
+        self.reduce_to_owner, self.pre_div = True, pre_div
+        numel = np.asarray(numel, np.int64)
+        self.flat_offset = np.concatenate([[0], np.cumsum(numel)[:-1]]).astype(np.int64)
+        total = int(numel.sum())
+        self.part_size = max(-(-total // world), 1)
+        self.parts = parts if parts is not None else \
+            [torch.empty(self.part_size, dtype=dtype, device="cuda") for _ in range(world)]
+        if len(self.parts) != world or any(p.numel() < self.part_size for p in self.parts):
+            raise ValueError(f"one partition buffer of {self.part_size} elements per rank")
+        self.buckets = [(int(s), np.ascontiguousarray(t, dtype=TASK_DTYPE)) for s, t in buckets]
+        self.sizes = [int((t["offset"] + t["numel"]).max()) if len(t) else 0 for _, t in self.buckets]
+        self.probe_log = probe_log
+        # a task is cut into at most (pieces it spans) destinations: n_tasks + world - 1 per bucket
+        ws = max((flush_workspace_bytes(world, len(t) + world) for _, t in self.buckets), default=0)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda") if ws else None
+        self.overlap = True
+        self._native = None
+        self._bound = None
+
+    def _create(self, grads, ld, nb, starts, counts, tasks, ws_ptr, ws_bytes, handle):
+        W = self.world
+        parts = (ctypes.c_void_p * W)(*[p.data_ptr() for p in self.parts])
+        _check(lib().dpred_executor_create_partitioned(W, _dtype_code(grads), self.dt_code, int(self.pre_div),
+                                                       grads.data_ptr(), ld, nb, starts.ctypes.data, counts.ctypes.data,
+                                                       tasks.ctypes.data, self.flat_offset.ctypes.data,
+                                                       len(self.flat_offset), self.part_size, parts, ws_ptr, ws_bytes,
+                                                       ctypes.byref(handle)))
+
+    def _regions(self):
+        return self.parts

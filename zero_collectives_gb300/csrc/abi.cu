@@ -406,11 +406,17 @@ static int partition_pieces(int32_t world, const dpred_task* tasks, int32_t n_ta
     return DPRED_OK;
 }
 
-int dpred_flush_bucket_partitioned(int32_t world, int32_t in_dtype, const void* grads, int64_t ld,
-                                   const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset,
-                                   int32_t n_params, int64_t part_size, int32_t out_dtype, void* const* part_dst,
-                                   int32_t pre_div, dpred_probe* probe, void* workspace, size_t workspace_bytes,
-                                   void* stream) {
+}  // extern "C"
+
+namespace dpred {
+
+// The plan and probe of one partitioned flush: validation, the pieces of every
+// task cut at the partition boundaries, and one destination per piece inside
+// its rank's partition buffer.  Shared by dpred_flush_bucket_partitioned and
+// the partitioned executor.
+int partitioned_plan(int32_t world, int32_t in_dtype, int32_t out_dtype, const void* grads, int64_t ld,
+                     const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset, int32_t n_params,
+                     int64_t part_size, void* const* part_dst, std::vector<Dest>& plan, dpred_probe* probe) {
     if (!dtype_ok(in_dtype) || !dtype_ok(out_dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
     if (ld < 0) return set_error(DPRED_E_INVAL, "ld < 0");
     int rc = validate_tasks(world, tasks, n_tasks, nullptr, 0, ld, true);
@@ -442,7 +448,7 @@ int dpred_flush_bucket_partitioned(int32_t world, int32_t in_dtype, const void* 
         for (const PartPiece& p : pieces)
             if (part_dst[p.rank]) probe->kept_elems[p.rank] += p.hi - p.lo;
     }
-    std::vector<Dest> plan;
+    plan.clear();
     plan.reserve(pieces.size());
     for (const PartPiece& p : pieces) {
         if (!part_dst[p.rank]) continue;
@@ -452,6 +458,22 @@ int dpred_flush_bucket_partitioned(int32_t world, int32_t in_dtype, const void* 
         d.ptrs.push_back(static_cast<char*>(part_dst[p.rank]) + (p.lo - p.rank * part_size) * osz);
         plan.push_back(std::move(d));
     }
+    return DPRED_OK;
+}
+
+}  // namespace dpred
+
+extern "C" {
+
+int dpred_flush_bucket_partitioned(int32_t world, int32_t in_dtype, const void* grads, int64_t ld,
+                                   const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset,
+                                   int32_t n_params, int64_t part_size, int32_t out_dtype, void* const* part_dst,
+                                   int32_t pre_div, dpred_probe* probe, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+    std::vector<Dest> plan;
+    int rc = partitioned_plan(world, in_dtype, out_dtype, grads, ld, tasks, n_tasks, flat_offset, n_params, part_size,
+                              part_dst, plan, probe);
+    if (rc) return rc;
     return run_plan(world, in_dtype, grads, ld, out_dtype, pre_div, plan, workspace, workspace_bytes,
                     static_cast<cudaStream_t>(stream));
 }

@@ -168,6 +168,13 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
 // that this flush shares no byte with the previous launch on the stream).
 int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl = false);
 
+// Validation, plan and probe of one partitioned flush (each task cut at the
+// partition boundaries of part_size elements; piece destinations inside the
+// ranks' partition buffers part_dst[world]).
+int partitioned_plan(int32_t world, int32_t in_dtype, int32_t out_dtype, const void* grads, int64_t ld,
+                     const dpred_task* tasks, int32_t n_tasks, const int64_t* flat_offset, int32_t n_params,
+                     int64_t part_size, void* const* part_dst, std::vector<Dest>& plan, dpred_probe* probe);
+
 int launch_flush_bf16_in(const FlushLaunch& L, cudaStream_t s);
 int launch_flush_f32_in(const FlushLaunch& L, cudaStream_t s);
 

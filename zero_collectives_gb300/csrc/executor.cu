@@ -28,6 +28,7 @@ struct dpred_executor {
     int world, in_dt, out_dt, pre_div;
     const char* grads;  // device [world, ld]
     int64_t ld;
+    std::vector<int64_t> bucket_start;            // as given at creation
     std::vector<int64_t> start, size;             // per bucket: column range of the gradient rows
     std::vector<dpred::BuiltPlan> plans;          // per bucket
     std::vector<dpred_probe> probes;              // per bucket (flush_index filled per call)
@@ -115,6 +116,78 @@ int flush_one(dpred_executor* ex, int b, dpred_probe* probe, void* stream, bool 
     return dpred::launch_plan(ex->plans[b], ex->workspace, ex->workspace_bytes, static_cast<cudaStream_t>(stream), pdl);
 }
 
+// A new executor with its arguments checked; buckets are added by add_bucket.
+int new_executor(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div, const void* grads, int64_t ld,
+                 int32_t n_buckets, const int64_t* bucket_start, const int32_t* bucket_tasks, void* workspace,
+                 size_t workspace_bytes, dpred_executor** out) {
+    using namespace dpred;
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (n_buckets < 0 || (n_buckets > 0 && (!bucket_start || !bucket_tasks)))
+        return set_error(DPRED_E_INVAL, "bad bucket list");
+    if ((in_dtype != DPRED_BF16 && in_dtype != DPRED_F32) || (out_dtype != DPRED_BF16 && out_dtype != DPRED_F32))
+        return set_error(DPRED_E_INVAL, "bad dtype");
+    if (ld < 0) return set_error(DPRED_E_INVAL, "ld < 0");
+    if (grads && reinterpret_cast<uintptr_t>(grads) % esz(in_dtype))
+        return set_error(DPRED_E_ALIGN, "grads not aligned to its element size");
+    for (int b = 0; b < n_buckets; ++b)
+        if (bucket_tasks[b] < 0) return set_error(DPRED_E_INVAL, "bucket %d: negative task count", b);
+    auto ex = new (std::nothrow) dpred_executor();
+    if (!ex) return set_error(DPRED_E_INVAL, "out of host memory");
+    ex->world = world;
+    ex->in_dt = in_dtype;
+    ex->out_dt = out_dtype;
+    ex->pre_div = pre_div;
+    ex->grads = static_cast<const char*>(grads);
+    ex->ld = ld;
+    ex->workspace = workspace;
+    ex->workspace_bytes = workspace_bytes;
+    ex->bucket_start.assign(bucket_start, bucket_start + n_buckets);
+    *out = ex;
+    return DPRED_OK;
+}
+
+// Bucket b: its tasks (for the column range) and its delivered destinations,
+// already validated.  Builds the launch plan and records what the bucket writes.
+int add_bucket(dpred_executor* ex, int b, const dpred_task* bt, int nt, std::vector<dpred::Dest>&& plan,
+               const dpred_probe& pr) {
+    using namespace dpred;
+    const int64_t start = ex->bucket_start[b];
+    int64_t width = 0;
+    for (int t = 0; t < nt; ++t) width = std::max(width, bt[t].offset + bt[t].numel);
+    if (start < 0 || start + width > ex->ld)
+        return set_error(DPRED_E_SIZE, "bucket %d: columns [%lld, %lld) outside the row of %lld", b, (long long)start,
+                         (long long)(start + width), (long long)ex->ld);
+    if (width > 0 && ex->grads == nullptr) return set_error(DPRED_E_INVAL, "null grads");
+    const int osz = esz(ex->out_dt);
+    std::vector<std::pair<char*, int64_t>> wr;
+    for (const Dest& d : plan)
+        for (void* p : d.ptrs) {
+            if (reinterpret_cast<uintptr_t>(p) % osz)
+                return set_error(DPRED_E_ALIGN, "bucket %d: destination not aligned to its element size", b);
+            if (d.numel > 0) wr.emplace_back(static_cast<char*>(p), d.numel * osz);
+        }
+    BuiltPlan bp;
+    build_plan(ex->world, ex->in_dt, ex->grads + start * esz(ex->in_dt), ex->ld, ex->out_dt, ex->pre_div, plan, bp);
+    if (bp.h.n_tasks > kInlineTasks || (int)bp.pool.size() > kInlineDst) {
+        const size_t need = sizeof(TaskDesc) * bp.tasks.size() + ((bp.pool.size() * sizeof(void*) + 15) & ~(size_t)15);
+        if (!ex->workspace || ex->workspace_bytes < need)
+            return set_error(DPRED_E_SIZE, "bucket %d needs %zu bytes of workspace, got %zu", b, need,
+                             ex->workspace_bytes);
+    }
+    ex->start.push_back(start);
+    ex->size.push_back(width);
+    ex->plans.push_back(std::move(bp));
+    ex->probes.push_back(pr);
+    ex->written.push_back(std::move(wr));
+    ex->dests.push_back(std::move(plan));
+    return DPRED_OK;
+}
+
+void finish_executor(dpred_executor* ex) {
+    ex->overlap_ok = buckets_independent(ex->start, ex->size, ex->dests, esz(ex->out_dt), ex->grads,
+                                         (int64_t)ex->world * ex->ld * esz(ex->in_dt));
+}
+
 void release(dpred_executor* ex) {
     if (ex->h2d) cudaStreamDestroy(ex->h2d);
     if (ex->d2h) cudaStreamDestroy(ex->d2h);
@@ -153,89 +226,75 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
     using namespace dpred;
     if (!out) return set_error(DPRED_E_INVAL, "null executor output");
     *out = nullptr;
-    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
-    if (n_buckets < 0 || (n_buckets > 0 && (!bucket_start || !bucket_tasks)))
-        return set_error(DPRED_E_INVAL, "bad bucket list");
-    auto ex = new (std::nothrow) dpred_executor();
-    if (!ex) return set_error(DPRED_E_INVAL, "out of host memory");
-    ex->world = world;
-    ex->in_dt = in_dtype;
-    ex->out_dt = out_dtype;
-    ex->pre_div = pre_div;
-    ex->grads = static_cast<const char*>(grads);
-    ex->ld = ld;
-    ex->workspace = workspace;
-    ex->workspace_bytes = workspace_bytes;
+    dpred_executor* ex = nullptr;
+    int rc = new_executor(world, in_dtype, out_dtype, pre_div, grads, ld, n_buckets, bucket_start, bucket_tasks,
+                          workspace, workspace_bytes, &ex);
+    if (rc) return rc;
+    if (dst == nullptr && n_buckets > 0) {
+        delete ex;
+        return set_error(DPRED_E_INVAL, "the executor needs destination tables");
+    }
     int64_t t0 = 0, d0 = 0;
     for (int b = 0; b < n_buckets; ++b) {
         const int nt = bucket_tasks[b];
-        if (nt < 0) {
-            delete ex;
-            return set_error(DPRED_E_INVAL, "bucket %d: negative task count", b);
-        }
         const dpred_task* bt = tasks + t0;
-        void* const* bd = dst ? dst + d0 : nullptr;
-        int64_t width = 0;
-        for (int t = 0; t < nt; ++t) width = std::max(width, bt[t].offset + bt[t].numel);
-        if (bucket_start[b] < 0 || bucket_start[b] + width > ld) {
-            delete ex;
-            return set_error(DPRED_E_SIZE, "bucket %d: columns [%lld, %lld) outside the row of %lld", b,
-                             (long long)bucket_start[b], (long long)(bucket_start[b] + width), (long long)ld);
-        }
+        void* const* bd = dst + d0;
         // Full validation through the public probe path (same rules as a flush).
         dpred_probe pr{};
-        int rc = dpred_flush_probe(world, bt, nt, owner, n_params, bd, reduce_to_owner, &pr);
-        if (rc == DPRED_OK && ((in_dtype != DPRED_BF16 && in_dtype != DPRED_F32) ||
-                               (out_dtype != DPRED_BF16 && out_dtype != DPRED_F32)))
-            rc = set_error(DPRED_E_INVAL, "bad dtype");
-        if (rc == DPRED_OK && dst == nullptr) rc = set_error(DPRED_E_INVAL, "the executor needs destination tables");
-        if (rc == DPRED_OK && width > 0 && grads == nullptr) rc = set_error(DPRED_E_INVAL, "null grads");
-        if (rc == DPRED_OK && grads && reinterpret_cast<uintptr_t>(grads) % esz(in_dtype))
-            rc = set_error(DPRED_E_ALIGN, "grads not aligned to its element size");
-        if (rc) {
-            delete ex;
-            return rc;
-        }
+        rc = dpred_flush_probe(world, bt, nt, owner, n_params, bd, reduce_to_owner, &pr);
         std::vector<Dest> plan(nt);
-        std::vector<std::pair<char*, int64_t>> wr;
-        for (int t = 0; t < nt; ++t) {
+        for (int t = 0; t < nt && rc == DPRED_OK; ++t) {
             const int root = (reduce_to_owner && owner && owner[bt[t].param_id] >= 0) ? owner[bt[t].param_id] : -1;
             plan[t].src_off = bt[t].offset;
             plan[t].numel = bt[t].numel;
             for (int r = 0; r < world; ++r) {
                 if (root >= 0 && r != root) continue;
                 void* p = bd[(int64_t)r * nt + t];
-                if (!p) continue;
-                if (reinterpret_cast<uintptr_t>(p) % esz(out_dtype)) {
-                    delete ex;
-                    return set_error(DPRED_E_ALIGN, "bucket %d: destination not aligned to its element size", b);
-                }
-                plan[t].ptrs.push_back(p);
-                if (bt[t].numel > 0) wr.emplace_back(static_cast<char*>(p), bt[t].numel * esz(out_dtype));
+                if (p) plan[t].ptrs.push_back(p);
             }
         }
-        BuiltPlan bp;
-        build_plan(world, in_dtype, static_cast<const char*>(grads) + bucket_start[b] * esz(in_dtype), ld, out_dtype,
-                   pre_div, plan, bp);
-        if (bp.h.n_tasks > kInlineTasks || (int)bp.pool.size() > kInlineDst) {
-            const size_t need = sizeof(TaskDesc) * bp.tasks.size() + ((bp.pool.size() * sizeof(void*) + 15) & ~(size_t)15);
-            if (!workspace || workspace_bytes < need) {
-                delete ex;
-                return set_error(DPRED_E_SIZE, "bucket %d needs %zu bytes of workspace, got %zu", b, need,
-                                 workspace_bytes);
-            }
+        if (rc == DPRED_OK) rc = add_bucket(ex, b, bt, nt, std::move(plan), pr);
+        if (rc) {
+            delete ex;
+            return rc;
         }
-        ex->start.push_back(bucket_start[b]);
-        ex->size.push_back(width);
-        ex->plans.push_back(std::move(bp));
-        ex->probes.push_back(pr);
-        ex->written.push_back(std::move(wr));
-        ex->dests.push_back(std::move(plan));
         t0 += nt;
         d0 += (int64_t)world * nt;
     }
-    ex->overlap_ok = buckets_independent(ex->start, ex->size, ex->dests, esz(out_dtype), grads,
-                                         (int64_t)world * ld * esz(in_dtype));
+    finish_executor(ex);
+    *out = ex;
+    return DPRED_OK;
+}
+
+int dpred_executor_create_partitioned(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div,
+                                      const void* grads, int64_t ld, int32_t n_buckets, const int64_t* bucket_start,
+                                      const int32_t* bucket_tasks, const dpred_task* tasks,
+                                      const int64_t* flat_offset, int32_t n_params, int64_t part_size,
+                                      void* const* part_dst, void* workspace, size_t workspace_bytes,
+                                      dpred_executor** out) {
+    using namespace dpred;
+    if (!out) return set_error(DPRED_E_INVAL, "null executor output");
+    *out = nullptr;
+    dpred_executor* ex = nullptr;
+    int rc = new_executor(world, in_dtype, out_dtype, pre_div, grads, ld, n_buckets, bucket_start, bucket_tasks,
+                          workspace, workspace_bytes, &ex);
+    if (rc) return rc;
+    int64_t t0 = 0;
+    for (int b = 0; b < n_buckets; ++b) {
+        const int nt = bucket_tasks[b];
+        const dpred_task* bt = tasks + t0;
+        dpred_probe pr{};
+        std::vector<Dest> plan;
+        rc = partitioned_plan(world, in_dtype, out_dtype, static_cast<const char*>(grads) + bucket_start[b] * esz(in_dtype),
+                              ld, bt, nt, flat_offset, n_params, part_size, part_dst, plan, &pr);
+        if (rc == DPRED_OK) rc = add_bucket(ex, b, bt, nt, std::move(plan), pr);
+        if (rc) {
+            delete ex;
+            return rc;
+        }
+        t0 += nt;
+    }
+    finish_executor(ex);
     *out = ex;
     return DPRED_OK;
 }
