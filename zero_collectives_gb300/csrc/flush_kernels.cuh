@@ -671,7 +671,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
 template <typename Tin, typename Tout>
 int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
     switch (L.h.world) {
-        case 2: return launch_flush_w<2, 4, Tin, Tout>(L, s);  // batch = flush_batch(world)
+        case 2: return launch_flush_w<2, 2, Tin, Tout>(L, s);  // batch = flush_batch(world)
         case 4: return launch_flush_w<4, 2, Tin, Tout>(L, s);
         case 8: return launch_flush_w<8, 1, Tin, Tout>(L, s);
         case 16: return launch_flush_w<16, 1, Tin, Tout>(L, s);
