@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="flush sweep: bucket sizes 1 KB-1 GB per replica, W in {2,4,8,16}, bf16/fp32, eager and "
                          "CUDA-graph replay; one JSON line per case")
+    ap.add_argument("--sweep-worlds", default="2,4,8,16", help="--sweep: world sizes to run (comma-separated)")
     ap.add_argument("--row", choices=["allgather", "reduce_scatter", "accumulate"], default=None,
                     help="time one other hot-path row alone (small profiling cases) and print its JSON line")
     ap.add_argument("--row-nodes", type=int, default=8)
@@ -99,7 +100,7 @@ class Clocks:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -119,7 +120,8 @@ class Clocks:
 
     def stop(self) -> dict:
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "mem_mhz": None, "mem_mhz_min": None,
+                    "reasons": ["nvidia-smi unavailable"], "samples": 0}
         time.sleep(0.1)
         self.proc.terminate()
         try:
@@ -130,17 +132,19 @@ class Clocks:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 9:
+                if len(parts) >= 10:
                     rows.append(parts)
         try:
             os.remove(self.path)
         except OSError:
             pass
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mem = [float(r[9]) for r in rows if r[9].replace(".", "").isdigit()]
         mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "mem_mhz": statistics.median(mem) if mem else None, "mem_mhz_min": min(mem) if mem else None,
                 "reasons": reasons, "samples": len(rows)}
 
 
@@ -913,7 +917,7 @@ def sweep(args):
     peak, _ = peaks()
     s = torch.cuda.current_stream()
     l2 = 129 * 2**20
-    for W in (2, 4, 8, 16):
+    for W in [int(w) for w in args.sweep_worlds.split(",")]:
         for dt, code in ((torch.bfloat16, BF16), (torch.float32, F32)):
             esize = 2 if code == BF16 else 4
             for kb in (1, 16, 256, 4096, 65536, 1048576):
@@ -946,18 +950,22 @@ def sweep(args):
                     for e, g in zip(exs, gs):
                         e.flush_all(g)
 
-                ms_e = timed(eager, reps // copies, warm=3) / copies
                 side = torch.cuda.Stream()
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=side):
                     eager()
+                clocks = Clocks(smi_gpu_id(torch.cuda.current_device()))
+                clocks.start()
+                ms_e = timed(eager, reps // copies, warm=3) / copies
                 ms_g = timed(graph.replay, reps // copies, warm=3) / copies
+                clk = clocks.stop()
                 line = {"sweep": True, "world": W, "dtype": "bf16" if code == BF16 else "f32",
                         "bucket_bytes_per_replica": full.total * esize, "elems": full.total, "copies": copies,
                         "bytes": nbytes, "eager_us": round(ms_e * 1e3, 2), "graph_us": round(ms_g * 1e3, 2),
                         "eager_GBps": round(nbytes / (ms_e * 1e-3) / 1e9, 1),
                         "graph_GBps": round(nbytes / (ms_g * 1e-3) / 1e9, 1),
-                        "graph_frac_of_peak": round(nbytes / (ms_g * 1e-3) / 1e9 / peak, 4)}
+                        "graph_frac_of_peak": round(nbytes / (ms_g * 1e-3) / 1e9 / peak, 4),
+                        "sm_mhz": clk["sm_mhz"], "mem_mhz_min": clk["mem_mhz_min"], "clock_reasons": clk["reasons"]}
                 print(json.dumps(line), flush=True)
                 for e in exs:
                     e.close()

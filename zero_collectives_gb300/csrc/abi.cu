@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -146,6 +147,24 @@ int sm_count() {
         cached[dev] = n;
     }
     return cached[dev];
+}
+
+int resident_ctas(const void* kernel, int threads) {
+    struct Entry {
+        const void* kernel;
+        int threads, dev, occ;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Entry& e : cache)
+        if (e.kernel == kernel && e.threads == threads && e.dev == dev) return e.occ;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, 0) != cudaSuccess || occ < 1) occ = 1;
+    cache.push_back(Entry{kernel, threads, dev, occ});
+    return occ;
 }
 
 int* device_error_word() {

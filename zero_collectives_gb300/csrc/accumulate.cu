@@ -150,9 +150,7 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const float* __restr
 
 template <typename K>
 unsigned grid_for(K kernel, int64_t work_items) {
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0) != cudaSuccess || occ < 1) occ = 1;
-    int64_t g = (int64_t)sm_count() * occ;
+    int64_t g = (int64_t)sm_count() * resident_ctas(reinterpret_cast<const void*>(kernel), kThreads);
     int64_t need = (work_items + kThreads - 1) / kThreads;
     if (need < 1) need = 1;
     return (unsigned)(need < g ? need : g);

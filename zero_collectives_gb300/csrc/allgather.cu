@@ -49,11 +49,9 @@ __global__ void __launch_bounds__(kThreads) allgather_kernel(const V* __restrict
 template <typename V>
 int launch_v(int n_nodes, int64_t shard_v, const void* in, void* out, int order, cudaStream_t s) {
     auto k = allgather_kernel<V>;
-    int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, kThreads, 0) != cudaSuccess || occ < 1) occ = 1;
     int64_t items = (int64_t)n_nodes * shard_v;
     int64_t need = (items + kThreads - 1) / kThreads;
-    int64_t g = (int64_t)sm_count() * occ;
+    int64_t g = (int64_t)sm_count() * resident_ctas(reinterpret_cast<const void*>(k), kThreads);
     if (need < g) g = need;
     if (g < 1) g = 1;
     k<<<(unsigned)g, kThreads, 0, s>>>(static_cast<const V*>(in), static_cast<V*>(out), n_nodes, shard_v, order);

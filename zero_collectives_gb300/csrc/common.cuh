@@ -26,6 +26,10 @@ int cuda_error(cudaError_t e, const char* what);
 // ----------------------------------------------------------- device info ---
 
 int sm_count();  // SMs of the current device (cached per device)
+// Resident CTAs per SM of `kernel` (any __global__ function) launched with
+// `threads` threads and no dynamic shared memory, on the current device;
+// queried once per (kernel, threads, device) and cached.  At least 1.
+int resident_ctas(const void* kernel, int threads);
 
 // Apply a kernel's dynamic shared-memory limit once per device; `done` is that
 // kernel's per-device flag array (the attribute is per device context).

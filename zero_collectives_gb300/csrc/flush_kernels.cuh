@@ -100,6 +100,10 @@ __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 #endif
 }
 
+#ifndef DPRED_FOLD_FMA
+#define DPRED_FOLD_FMA 0
+#endif
+
 // Fold one replica's vector into the running sums (rank order is the call order).
 template <typename Tin, int MODE>
 __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q, bool first, float wf, float inv_w) {
@@ -108,8 +112,16 @@ __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q
     unpack<Tin>(q, f);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
-        float t = pre_divide(f[j], MODE, wf, inv_w);
-        y[j] = first ? t : __fadd_rn(y[j], t);
+        if constexpr (DPRED_FOLD_FMA && std::is_same<Tin, __nv_bfloat16>::value && MODE == PDIV_POW2) {
+            // x * 2^-k is exact for a bf16 x (8 significant bits, lowest bit at
+            // 2^-133 or above) and 2^k <= 64 ranks, so rounding x * inv_w + y
+            // once is the same as rounding the quotient's sum: one fused step
+            // instead of a multiply and an add, with identical bits.
+            y[j] = first ? __fmul_rn(f[j], inv_w) : __fmaf_rn(f[j], inv_w, y[j]);
+        } else {
+            float t = pre_divide(f[j], MODE, wf, inv_w);
+            y[j] = first ? t : __fadd_rn(y[j], t);
+        }
     }
 }
 
@@ -577,16 +589,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) flush_tma_kernel(const __grid_
         tma_consume<W_T, Tin, Tout, PDIV_NONE>(a, smem, full, empty, &abort_flag);
 }
 
-// Persistent grid: SMs x resident CTAs (queried once per kernel), capped by the number of units.
+// Persistent grid: SMs x resident CTAs of this kernel, capped by the number of units.
 template <typename K>
 int64_t persistent_grid(K kernel, int64_t units) {
-    static int occ = 0;
-    if (occ == 0) {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kFlushThreads, 0) != cudaSuccess || o < 1) o = 1;
-        occ = o;
-    }
-    int64_t g = (int64_t)sm_count() * occ;
+    int64_t g = (int64_t)sm_count() * resident_ctas(reinterpret_cast<const void*>(kernel), kFlushThreads);
     return units < g ? units : g;
 }
 

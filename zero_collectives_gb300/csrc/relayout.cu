@@ -77,13 +77,7 @@ __global__ void __launch_bounds__(kThreads) copy_kernel(const __grid_constant__ 
 
 template <typename K>
 unsigned grid_for(K kernel, int64_t units) {
-    static int occ = 0;
-    if (occ == 0) {
-        int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kThreads, 0) != cudaSuccess || o < 1) o = 1;
-        occ = o;
-    }
-    int64_t g = (int64_t)sm_count() * occ;
+    int64_t g = (int64_t)sm_count() * resident_ctas(reinterpret_cast<const void*>(kernel), kThreads);
     return (unsigned)(units < g ? units : g);
 }
 
