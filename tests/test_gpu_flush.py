@@ -160,6 +160,38 @@ def test_in_place(rto, dt):
     assert probe.kept_elems == oprobe["kept_elems"]
 
 
+@pytest.mark.parametrize("world", [2, 3, 4, 8, 16, 64])
+def test_every_bf16_pattern(world):
+    """All 65,536 bf16 bit patterns (subnormals, signed zeros, infinities,
+    NaNs), rotated differently in every replica row, plus a block of columns
+    drawn only from subnormals and the smallest normals, so that pre-divided
+    terms sit at the bottom of the fp32 range.  In-place AllReduce form,
+    pre-division on: every row must equal the oracle bit for bit (a NaN only
+    has to stay NaN: the kernel's conversion returns a canonical NaN)."""
+    pats = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    tiny = np.concatenate([np.arange(0x0000, 0x0100), np.arange(0x8000, 0x8100)]).astype(np.uint16)
+    rng = np.random.default_rng(world)
+    n = len(pats) + 4096
+    host = np.empty((world, n), np.uint16)
+    for r in range(world):
+        host[r, :len(pats)] = np.roll(pats, r * 7919)
+        host[r, len(pats):] = rng.choice(tiny, 4096)
+    grads = torch.from_numpy(host.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    tasks = np.zeros(1, dtype=zc.TASK_DTYPE)
+    tasks["numel"] = n
+    zc.flush_bucket(grads, tasks, None, None, BF16, True, False)
+    oracle.flush(world, host, tasks, None, 1, None, BF16, True, False)
+    torch.cuda.synchronize()
+    got = to_bits(grads)
+
+    def nan(b):
+        return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
+
+    same = (got == host) | (nan(got) & nan(host))
+    assert same.all(), f"{int((~same).sum())} elements differ, first at {np.argwhere(~same)[0]}"
+    assert zc.device_status() == 0
+
+
 def test_identical_replicas_reproduce_exactly():
     """The DeepSpeed issue's exactness check: identical input on every rank
     reproduces the input exactly (bf16, pre-division by a power of two)."""

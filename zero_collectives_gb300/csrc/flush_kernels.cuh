@@ -100,10 +100,6 @@ __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 #endif
 }
 
-#ifndef DPRED_FOLD_FMA
-#define DPRED_FOLD_FMA 0
-#endif
-
 // Fold one replica's vector into the running sums (rank order is the call order).
 template <typename Tin, int MODE>
 __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q, bool first, float wf, float inv_w) {
@@ -112,11 +108,13 @@ __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q
     unpack<Tin>(q, f);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
-        if constexpr (DPRED_FOLD_FMA && std::is_same<Tin, __nv_bfloat16>::value && MODE == PDIV_POW2) {
+        if constexpr (std::is_same<Tin, __nv_bfloat16>::value && MODE == PDIV_POW2) {
             // x * 2^-k is exact for a bf16 x (8 significant bits, lowest bit at
-            // 2^-133 or above) and 2^k <= 64 ranks, so rounding x * inv_w + y
-            // once is the same as rounding the quotient's sum: one fused step
-            // instead of a multiply and an add, with identical bits.
+            // 2^-133 or above; 2^-133 * 2^-6 is still a multiple of the smallest
+            // fp32 subnormal 2^-149) and 2^k <= 64 ranks.  So rounding
+            // x * inv_w + y once gives the bits of rounding y + (x / W): one
+            // fused step instead of a multiply and an add.  fp32 inputs keep
+            // the two steps, since their quotient can be inexact.
             y[j] = first ? __fmul_rn(f[j], inv_w) : __fmaf_rn(f[j], inv_w, y[j]);
         } else {
             float t = pre_divide(f[j], MODE, wf, inv_w);
