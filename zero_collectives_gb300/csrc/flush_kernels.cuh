@@ -90,13 +90,20 @@ __device__ __forceinline__ void store_vec<float, 4>(float* p, const float (&y)[4
     __stcs(reinterpret_cast<float4*>(p), make_float4(y[0], y[1], y[2], y[3]));
 }
 
-// A 16-byte streaming load that a checked build skips (reads zeros) when its
-// bounds test failed; see access_ok.
+// A 16-byte load of a replica row that a checked build skips (reads zeros)
+// when its bounds test failed; see access_ok.  Rows are loaded cached in L2
+// at normal priority (ld.global.cg); results are stored evict-first
+// (st.global.cs).  Interleaved A/B runs on GB300, against evict-first (.cs)
+// loads: 3-7% faster on buckets of 512 MB and more (ReduceScatter of 1 GiB
+// rows, single large buckets), equal on the 805 MB buckets of the 402.8M
+// model, 1.5-1.8% slower on buckets of 34-64 MB.  Non-coherent loads and
+// loads with an L2 256-byte prefetch hint were no better; plain and .cg stores
+// were 3-7% slower than .cs stores.
 __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 #if DPRED_CHECKED
-    return ok ? __ldcs(p) : make_uint4(0u, 0u, 0u, 0u);
+    return ok ? __ldcg(p) : make_uint4(0u, 0u, 0u, 0u);
 #else
-    return __ldcs(p);
+    return __ldcg(p);
 #endif
 }
 
