@@ -351,13 +351,17 @@ def e2e(args, ex, grads, step_bytes, ws):
     for f in forms.values():
         f()
     torch.cuda.synchronize()
-    # the host link's own bandwidth in this run, for context: one plain copy
-    c0, c1 = events(2)
-    c0.record(stream)
-    grads.copy_(host, non_blocking=True)
-    c1.record(stream)
+    # the host link's own bandwidth in this run, for context: the median of
+    # five plain copy-engine copies (single copies from pinned host memory
+    # occasionally take two to three times as long on this platform)
+    evs = events(6)
+    evs[0].record(stream)
+    for i in range(5):
+        grads.copy_(host, non_blocking=True)
+        evs[i + 1].record(stream)
     torch.cuda.synchronize()
-    link_gbs = host.numel() * host.element_size() / (c0.elapsed_time(c1) * 1e-3) / 1e9
+    copy_ms = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(5))
+    link_gbs = host.numel() * host.element_size() / (copy_ms[2] * 1e-3) / 1e9
     ms = {}
     for name, f in forms.items():
         barrier(ws)
