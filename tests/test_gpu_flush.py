@@ -252,6 +252,67 @@ def test_402m_w8_full_size_sampled():
     assert sum(p.reduced_elems for p in probes) == tree.total
 
 
+@pytest.mark.parametrize("world,dt", [(2, BF16), (16, BF16), (8, F32)])
+def test_sweep_1gb_per_replica_sampled(world, dt):
+    """The largest sweep case (1 GB per replica row) in the layout the sweep
+    times: one bucket whose W-1 interior partition boundaries all fall inside
+    a parameter, plus a 3-parameter group on a smaller communicator (AllReduce
+    to every rank), flushed through the executor.  Every delivered slot is
+    fully written and nothing else; sampled values (both ends of every
+    parameter, the elements around every partition boundary and random ones)
+    equal the oracle bit for bit."""
+    esize = 2 if dt == BF16 else 4
+    seed, sigma = 6, 1e-3
+    tree = workloads.straddle_tree(world, (1 << 30) // esize, world - 1, pieces=2)
+    ex_sizes = np.array([96, 64, 32], np.int64)
+    numel = np.concatenate([tree.numel, ex_sizes])
+    full = workloads.Tree([f"p{i}" for i in range(len(numel))], numel)
+    layout = workloads.arrival_layout(full, capacity=None)
+    sub = list(range(max(1, world // 2)))
+    grads = device_matrix(world, full.total, dt, NORMAL, seed, sigma=sigma)
+    ex = zc.Zero1Executor(world, numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets], TORCH_DT[dt],
+                          groups=[(None, tree.numel), (sub, ex_sizes)], fill=float("nan"))
+    ex.flush_all(grads)
+    torch.cuda.synchronize()
+    assert zc.device_status() == 0
+    om = oracle.owner_map(world, [(list(range(world)), tree.numel), (sub, ex_sizes)])
+    assert np.array_equal(om["owner"], ex.omap.owner)
+    holders = holder_sets(om["holder_lo"], om["holder_hi"])
+    delivered = [[p for p in range(full.n_params) if (om["owner"][p] == r or (om["owner"][p] < 0 and r in holders[p]))]
+                 for r in range(world)]
+    for r in range(world):
+        want = sum(int(numel[p]) for p in delivered[r])
+        written = int((~torch.isnan(ex.grad.buf[r].float())).sum().item())
+        assert written == want, f"rank {r}: {written} written, {want} delivered"
+    del grads
+    # samples: parameter ends, +-2 elements around every partition boundary, random
+    rng = np.random.default_rng(world)
+    T = int(tree.numel.sum())
+    part = -(-T // world)
+    flat0 = np.concatenate([[0], np.cumsum(numel)[:-1]])
+    picks = set()
+    for p in range(full.n_params):
+        n = int(numel[p])
+        picks |= {(p, 0), (p, n - 1)} | {(p, int(k)) for k in rng.integers(0, n, size=16)}
+    for b in range(1, world):
+        for f in range(b * part - 2, b * part + 2):
+            p = int(np.searchsorted(flat0[:tree.n_params], f, side="right") - 1)
+            if 0 <= f - flat0[p] < numel[p]:
+                picks.add((p, int(f - flat0[p])))
+    picks = sorted(picks)
+    P = np.array([p for p, _ in picks])
+    K = np.array([k for _, k in picks])
+    cols = layout.row_offset[P] + K
+    x = np.stack([datagen.sample_host(np.full(len(cols), r), cols, dt, NORMAL, seed, sigma) for r in range(world)])
+    want = np_bits(oracle.reduce_rows(x, pre_div=True))
+    for r in range(world):
+        sel = [i for i, p in enumerate(P) if p in set(delivered[r])]
+        idx = torch.tensor([ex.grad.slot[r][int(P[i])] + int(K[i]) for i in sel], device="cuda")
+        got = to_bits(ex.grad.buf[r][idx])
+        assert np.array_equal(got, want[sel]), f"rank {r}"
+    ex.close()
+
+
 def test_indices_beyond_int32():
     """A task longer than 2^31 elements and a task that starts past element
     2^31 of its row: every 64-bit index path (unit search, vector and scalar
