@@ -120,6 +120,22 @@ struct FlushArgsWs {
 };
 
 constexpr int kFlushThreads = 256;
+// Resident flush CTAs per SM: the persistent grid is capped at this many per
+// SM, and the kernels of these world sizes are compiled to fit them.  Measured
+// by interleaved A/B on GB300 with the grid capped at 2, 3 or 4 CTAs per SM:
+// - W=8: 3 is 3-5% faster than 4 on ReduceScatter of 1 GiB rows and on single
+//   buckets of 512 MB and more, within 0.5% on the 402.8M step, and 1.8%
+//   slower on a step of 98 small buckets; 2 is slower everywhere.  W=4
+//   follows W=8 (same loads in flight per thread: 4 rows x 2 vectors).
+// - W=2 keeps only 2 x 2 loads in flight per thread and needs 4 CTAs: capped
+//   at 3 it lost 7% on 1 GB buckets.
+// W=16 and the generic world size keep what their registers allow (2).
+__host__ __device__ constexpr int flush_ctas_per_sm(int w) { return w == 2 ? 4 : (w == 4 || w == 8) ? 3 : 16; }
+// The matching __launch_bounds__ minimum (0 = none).  Without a bound the
+// W=8 kernel's register count moved between 56 and 89 with small source
+// changes, i.e. between 4 and 2 resident CTAs; an explicit minimum of 1 also
+// changes the allocation, so the other world sizes pass 0.
+__host__ __device__ constexpr int flush_min_blocks(int w) { return (w == 2 || w == 4 || w == 8) ? flush_ctas_per_sm(w) : 0; }
 constexpr int kUnitVec = 256;      // 16-byte vectors per thread-block pass of the vector path (4 KB per row)
 constexpr int kUnitScalar = 2048;  // elements per work unit of the scalar path
 

@@ -93,12 +93,12 @@ __device__ __forceinline__ void store_vec<float, 4>(float* p, const float (&y)[4
 // A 16-byte load of a replica row that a checked build skips (reads zeros)
 // when its bounds test failed; see access_ok.  Rows are loaded cached in L2
 // at normal priority (ld.global.cg); results are stored evict-first
-// (st.global.cs).  Interleaved A/B runs on GB300, against evict-first (.cs)
-// loads: 3-7% faster on buckets of 512 MB and more (ReduceScatter of 1 GiB
-// rows, single large buckets), equal on the 805 MB buckets of the 402.8M
-// model, 1.5-1.8% slower on buckets of 34-64 MB.  Non-coherent loads and
-// loads with an L2 256-byte prefetch hint were no better; plain and .cg stores
-// were 3-7% slower than .cs stores.
+// (st.global.cs).  Interleaved A/B on GB300 at the same occupancy (3 CTAs per
+// SM, W=8) against evict-first (.cs) loads: 3.7% faster on 64 MB-per-replica
+// buckets, within 0.5% on the 402.8M step, ReduceScatter and 1 GB buckets,
+// 1.4% slower on a step of 98 small buckets.  Non-coherent loads and L2
+// 256-byte prefetch hints were no better; plain and .cg stores were 3-7%
+// slower than .cs stores.
 __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 #if DPRED_CHECKED
     return ok ? __ldcg(p) : make_uint4(0u, 0u, 0u, 0u);
@@ -406,7 +406,7 @@ __device__ __forceinline__ int find_task(const Args& a, int64_t u) {
 // idle, and still completes after it, so the stream's order of completion is
 // unchanged.  Launched without the attribute, both instructions do nothing.
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args, bool RA>
-__global__ void __launch_bounds__(kFlushThreads) flush_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kFlushThreads, flush_min_blocks(W_T)) flush_kernel(const __grid_constant__ Args a) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const FlushHeader& h = a.h;
     for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
@@ -596,8 +596,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1) flush_tma_kernel(const __grid_
 
 // Persistent grid: SMs x resident CTAs of this kernel, capped by the number of units.
 template <typename K>
-int64_t persistent_grid(K kernel, int64_t units) {
-    int64_t g = (int64_t)sm_count() * resident_ctas(reinterpret_cast<const void*>(kernel), kFlushThreads);
+int64_t persistent_grid(K kernel, int64_t units, int max_per_sm) {
+    int occ = resident_ctas(reinterpret_cast<const void*>(kernel), kFlushThreads);
+    if (occ > max_per_sm) occ = max_per_sm;
+    int64_t g = (int64_t)sm_count() * occ;
     return units < g ? units : g;
 }
 
@@ -607,8 +609,8 @@ int64_t persistent_grid(K kernel, int64_t units) {
 // reach pinned host memory over the host link, and no bulk copy is issued there.
 // Launch of the LDG kernel, with programmatic stream serialisation when pdl.
 template <typename K, typename Args>
-cudaError_t launch_ldg(K k, const Args& a, int64_t units, bool pdl, cudaStream_t s) {
-    const unsigned grid = (unsigned)persistent_grid(k, units);
+cudaError_t launch_ldg(K k, const Args& a, int64_t units, int max_per_sm, bool pdl, cudaStream_t s) {
+    const unsigned grid = (unsigned)persistent_grid(k, units, max_per_sm);
     if (!pdl) {
         k<<<grid, kFlushThreads, 0, s>>>(a);
         return cudaGetLastError();
@@ -641,9 +643,10 @@ cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_o
         }
     }
     if constexpr (std::is_same<Tin, Tout>::value) {
-        if (realign) return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, pdl, s);
+        if (realign)
+            return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, flush_ctas_per_sm(W_T), pdl, s);
     }
-    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, pdl, s);
+    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, flush_ctas_per_sm(W_T), pdl, s);
 }
 
 template <int W_T, int BATCH, typename Tin, typename Tout>
