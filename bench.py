@@ -304,7 +304,8 @@ def run_dpred(args):
     peak, peak_src = peaks()
     bytes_per_launch = step_bytes / launches_per_step
     achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
-    traffic = traffic_per_launch()
+    # the recorded traffic is per launch of the full 7-bucket workload
+    traffic = traffic_per_launch() if args.max_buckets <= 0 else None
     result = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps, 4), "higher_is_better": True,
