@@ -163,9 +163,17 @@ __global__ void __launch_bounds__(kThreads) finalize_kernel(const float* __restr
     }
 }
 
+// Resident CTAs per SM of the micro-batch add (grid cap).  Interleaved A/B on
+// GB300 with the grid capped at 1, 2, 3 or 4 CTAs per SM (4 fit): 2 is best,
+// 1.007 of the measured copy peak on the 402.8M W=8 bf16 add (0.788, 0.981,
+// 0.973 at 1, 3, 4) and 1.008 on the qwen3 W=4 fp32 add (0.871, 0.994, 0.990).
+// The finalize pass keeps full occupancy (capped at 2 it fell to 0.58).
+constexpr int kAccAddCtasPerSm = 2;
 template <typename K>
-unsigned grid_for(K kernel, int64_t work_items) {
-    int64_t g = (int64_t)sm_count() * resident_ctas(reinterpret_cast<const void*>(kernel), kThreads);
+unsigned grid_for(K kernel, int64_t work_items, int max_per_sm = 1 << 30) {
+    int occ = resident_ctas(reinterpret_cast<const void*>(kernel), kThreads);
+    if (occ > max_per_sm) occ = max_per_sm;
+    int64_t g = (int64_t)sm_count() * occ;
     int64_t need = (work_items + kThreads - 1) / kThreads;
     if (need < 1) need = 1;
     return (unsigned)(need < g ? need : g);
@@ -204,10 +212,10 @@ int launch_typed(int world, int64_t n, float* acc, const Tg* g, int first, int f
         int64_t items = vec ? total_elems / 4 : total_elems;
         if (first) {
             auto k = accumulate_kernel<Tg, true>;
-            k<<<grid_for(k, items), kThreads, 0, s>>>(acc, g, total_elems, vec);
+            k<<<grid_for(k, items, kAccAddCtasPerSm), kThreads, 0, s>>>(acc, g, total_elems, vec);
         } else {
             auto k = accumulate_kernel<Tg, false>;
-            k<<<grid_for(k, items), kThreads, 0, s>>>(acc, g, total_elems, vec);
+            k<<<grid_for(k, items, kAccAddCtasPerSm), kThreads, 0, s>>>(acc, g, total_elems, vec);
         }
     } else {
         // per column: every row start must keep the vector alignment
