@@ -30,6 +30,8 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     out.tasks.clear();
     out.pool.clear();
     out.realign = false;
+    out.write_heavy = false;
+    int64_t read_bytes = 0, write_bytes = 0;
     out.tasks.reserve(tasks.size());
     int64_t units = 0;
     const int unit_vec = kUnitVec * flush_batch(world);
@@ -70,7 +72,10 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
         units += flush_task_units(t, vec_elems, unit_vec);
         out.pool.insert(out.pool.end(), d.ptrs.begin(), d.ptrs.end());
         out.tasks.push_back(t);
+        read_bytes += (int64_t)world * d.numel * isz;
+        write_bytes += (int64_t)d.ptrs.size() * d.numel * osz;
     }
+    out.write_heavy = 2 * write_bytes >= read_bytes && read_bytes > 0;
     out.h = FlushHeader{};
     out.h.grads = grads;
     out.h.ld = ld;
@@ -100,6 +105,7 @@ int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cud
     L.realign = p.realign;
     L.ldg_only = p.ldg_only;
     L.pdl = pdl;
+    L.write_heavy = p.write_heavy;
     return p.in_dt == DPRED_BF16 ? launch_flush_bf16_in(L, s) : launch_flush_f32_in(L, s);
 }
 

@@ -131,6 +131,14 @@ constexpr int kFlushThreads = 256;
 //   at 3 it lost 7% on 1 GB buckets.
 // W=16 and the generic world size keep what their registers allow (2).
 __host__ __device__ constexpr int flush_ctas_per_sm(int w) { return w == 2 ? 4 : (w == 4 || w == 8) ? 3 : 16; }
+// Launches that write at least half as many bytes as they read (an AllReduce
+// delivered to every rank) run 2 CTAs per SM at W=4 and W=8: in place at W=8,
+// 0.952 of peak against 0.915 at 3 CTAs, while the owner form (writes about a
+// third of the reads) was 6% slower at 2.
+inline int flush_ctas_per_sm(int w, bool write_heavy) {
+    const int c = flush_ctas_per_sm(w);
+    return (write_heavy && (w == 4 || w == 8)) ? 2 : c;
+}
 // The matching __launch_bounds__ minimum (0 = none).  Without a bound the
 // W=8 kernel's register count moved between 56 and 89 with small source
 // changes, i.e. between 4 and 2 resident CTAs; an explicit minimum of 1 also
@@ -150,6 +158,7 @@ struct FlushLaunch {
     bool realign;            // some task takes the realigned vector path
     bool ldg_only;           // register streaming only: an operand lives in host memory
     bool pdl;                // may overlap the previous launch on the stream (disjoint buckets only)
+    bool write_heavy;        // the launch writes at least half as many bytes as it reads
 };
 
 // Vectors each thread keeps in flight per replica row: small world sizes take
@@ -178,6 +187,7 @@ struct BuiltPlan {
     int in_dt, out_dt;
     bool realign = false;
     bool ldg_only = false;  // gradients or destinations in pinned host memory
+    bool write_heavy = false;  // destination bytes >= half the replica-row bytes read
     std::vector<TaskDesc> tasks;
     std::vector<void*> pool;
 };

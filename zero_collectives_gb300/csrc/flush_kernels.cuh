@@ -629,7 +629,9 @@ cudaError_t launch_ldg(K k, const Args& a, int64_t units, int max_per_sm, bool p
 }
 
 template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
-cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_only, bool pdl, cudaStream_t s) {
+cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_only, bool write_heavy, bool pdl,
+                          cudaStream_t s) {
+    const int cap = flush_ctas_per_sm(W_T, write_heavy);
     if constexpr (W_T > 0) {
         if (!ldg_only && flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
             auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
@@ -644,9 +646,9 @@ cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_o
     }
     if constexpr (std::is_same<Tin, Tout>::value) {
         if (realign)
-            return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, flush_ctas_per_sm(W_T), pdl, s);
+            return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, cap, pdl, s);
     }
-    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, flush_ctas_per_sm(W_T), pdl, s);
+    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, cap, pdl, s);
 }
 
 template <int W_T, int BATCH, typename Tin, typename Tout>
@@ -659,7 +661,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.h = h;
         for (int i = 0; i < h.n_tasks; ++i) a.tasks[i] = L.tasks[i];
         for (int i = 0; i < L.n_dst; ++i) a.dst[i] = L.dst[i];
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, L.pdl, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, L.write_heavy, L.pdl, s);
     } else {
         size_t tb = sizeof(TaskDesc) * (size_t)h.n_tasks, db = sizeof(void*) * (size_t)L.n_dst;
         size_t need = tb + ((db + 15) & ~(size_t)15);
@@ -677,7 +679,7 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
         a.tasks = reinterpret_cast<const TaskDesc*>(ws);
         a.dst = reinterpret_cast<void* const*>(ws + tb);
         // the plan upload sits between this launch and the previous one: no overlap
-        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, false, s);
+        e = launch_kernel<W_T, BATCH, Tin, Tout>(a, h.total_units, L.realign, L.ldg_only, L.write_heavy, false, s);
     }
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
 }
