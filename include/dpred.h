@@ -284,6 +284,13 @@ int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int
  *     the first call that uses them and reused while they stay the same.
  *     host_ld must cover every bucket's columns (DPRED_E_SIZE).
  *   dpred_executor_destroy:   release the executor (after its work is done).
+ * In place: dst == NULL makes every flush write its delivered results back
+ * into the gradient rows themselves, as dpred_flush_bucket does without a
+ * destination table (row owner(t) for an owned parameter, every row for an
+ * AllReduce one).  It needs out_dtype == in_dtype (else DPRED_E_INVAL) and
+ * no two tasks of a bucket overlapping (else DPRED_E_SIZE).  Its probes
+ * count what each row received.  The host-buffer steps need destination
+ * buffers and return DPRED_E_INVAL on an in-place executor.
  */
 typedef struct dpred_executor dpred_executor;
 int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, int32_t pre_div, int32_t reduce_to_owner,
@@ -313,7 +320,8 @@ int dpred_executor_flush_all(dpred_executor* ex, dpred_probe* probes, void* stre
 /*
  * Launch overlap (no counterpart in the pages).  When no two buckets of the
  * executor can touch the same byte (disjoint column ranges, no two
- * destination ranges overlapping, no destination inside the gradient array;
+ * destination ranges overlapping, no destination inside the gradient array
+ * except in place, inside its own bucket's columns of one row;
  * checked once at creation, and for the mapped step whenever its host
  * pointers change), dpred_executor_flush_all and _flush_all_mapped launch
  * every flush after the first with programmatic stream serialisation: it

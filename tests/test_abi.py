@@ -241,9 +241,43 @@ def test_executor_create_validates_and_destroys_without_a_gpu(L):
                                    counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == -1
     assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, 0x10000, 100, 1, starts.ctypes.data,
                                    counts.ctypes.data, tasks.ctypes.data, dst, None, 0, ctypes.byref(h)) == -3
-    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 2, 0x10000, 128, 1, starts.ctypes.data,
+    # no destination table: in place, which needs the output dtype to be the input dtype
+    assert L.dpred_executor_create(world, 0, 1, 1, 1, owner.ctypes.data, 2, 0x10000, 128, 1, starts.ctypes.data,
                                    counts.ctypes.data, tasks.ctypes.data, None, None, 0, ctypes.byref(h)) == -1
     assert L.dpred_executor_flush(None, 0, None, None) == -1
+
+
+def test_in_place_executor_without_a_gpu(L):
+    """dst == NULL: results go back into the gradient rows.  Host plans only:
+    validation, overlap eligibility and the refusal of host-buffer steps."""
+    world, grads, ld = 4, 0x10000, 256
+    owner = np.array([0, -1, 2], np.int32)
+    tasks = _tasks([(0, 0, 64), (1, 64, 32), (2, 0, 100)])
+    starts = np.array([0, 96], np.int64)
+    counts = np.array([2, 1], np.int32)
+    h = ctypes.c_void_p()
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 3, grads, ld, 2, starts.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, None, None, 0, ctypes.byref(h)) == 0
+    assert L.dpred_executor_overlap_eligible(h) == 1     # in-place writes stay in each bucket's own columns
+    reg_dev = (ctypes.c_void_p * 1)(grads)
+    reg_host = (ctypes.c_void_p * 1)(0x300000)
+    nbytes = np.array([world * ld * 2], np.int64)
+    assert L.dpred_executor_flush_all_from_host(h, 0x400000, ld, 1, reg_dev, reg_host, nbytes.ctypes.data, None,
+                                                None) == -1
+    assert L.dpred_executor_flush_all_mapped(h, 0x400000, ld, 1, reg_dev, reg_host, nbytes.ctypes.data, None,
+                                             None) == -1
+    assert "in-place" in L.dpred_last_error().decode()
+    assert L.dpred_executor_destroy(h) == 0
+    # two tasks of one bucket sharing columns cannot both be written in place
+    overlapping = _tasks([(0, 0, 64), (1, 32, 32), (2, 0, 100)])
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 3, grads, ld, 2, starts.ctypes.data,
+                                   counts.ctypes.data, overlapping.ctypes.data, None, None, 0, ctypes.byref(h)) == -3
+    # bucket columns overlapping: allowed, but never overlapped on the GPU
+    starts2 = np.array([0, 64], np.int64)
+    assert L.dpred_executor_create(world, 0, 0, 1, 1, owner.ctypes.data, 3, grads, ld, 2, starts2.ctypes.data,
+                                   counts.ctypes.data, tasks.ctypes.data, None, None, 0, ctypes.byref(h)) == 0
+    assert L.dpred_executor_overlap_eligible(h) == 0
+    assert L.dpred_executor_destroy(h) == 0
 
 
 def test_flush_path_and_pipeline_argument_errors(L):
@@ -297,7 +331,9 @@ def test_executor_overlap_eligibility(L):
 
     assert eligible(64, 0x200000) == 1
     assert eligible(32, 0x200000) == 0              # bucket columns [0, 64) and [32, 96) overlap
-    assert eligible(64, grads + 512) == 0           # a destination inside the gradient array
+    assert eligible(64, grads + 512) == 0           # inside the gradient array, outside bucket 1's columns
+    assert eligible(64, grads + 512 + 128) == 1     # inside the gradient array, in bucket 1's own columns (in place)
+    assert eligible(64, grads + 512 + 130) == 0     # ... but running past them
     assert eligible(64, 0x100000 + 64) == 0         # bucket 1 writes into bucket 0's destination
     assert eligible(64, 0x100000 + 128) == 1        # adjacent, not overlapping
     assert L.dpred_executor_overlap_eligible(None) == -1

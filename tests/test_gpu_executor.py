@@ -9,7 +9,7 @@ import torch
 import datagen
 import zero_collectives_gb300 as zc
 from datagen import BF16, F32, NORMAL, workloads
-from tests.gpu_util import TORCH_DT, device_matrix
+from tests.gpu_util import TORCH_DT, device_matrix, to_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -192,4 +192,48 @@ def test_overlapped_launches_equal_serial_and_keep_stream_order(world):
         for r in range(world):
             assert torch.equal(after[r].view(torch.int16), serial[r].view(torch.int16))
     assert zc.device_status() == 0
+    ex.close()
+
+
+@pytest.mark.parametrize("overlap", [True, False])
+@pytest.mark.parametrize("rto", [True, False])
+@pytest.mark.parametrize("world,dt", [(8, torch.bfloat16), (4, torch.float32), (3, torch.bfloat16)])
+def test_in_place_executor_matches_the_oracle(world, dt, rto, overlap):
+    """The in-place executor step (no destination tables): every bucket's
+    delivered results land in the gradient rows themselves, bit for bit as the
+    oracle's in-place flush computes them, with W-1 straddlers and an
+    excluded group; the probes count what each row received."""
+    import oracle
+    code = BF16 if dt == torch.bfloat16 else F32
+    tree = workloads.straddle_tree(world, 30000 * world + 77, world - 1, pieces=4)
+    ex_sizes = np.array([96, 64, 40], np.int64)
+    numel = np.concatenate([tree.numel, ex_sizes])
+    full = workloads.Tree([f"p{i}" for i in range(len(numel))], numel)
+    layout = workloads.arrival_layout(full, capacity=full.total // 3)
+    assert len(layout.buckets) >= 3
+    sub = list(range(max(1, world // 2)))
+    groups = [(None, tree.numel), (sub, ex_sizes)]
+    grads = device_matrix(world, full.total, code, NORMAL, 13, sigma=1e-2)
+    host = datagen.host_matrix(world, full.total, code, NORMAL, 13, sigma=1e-2)
+    ex = zc.InPlaceExecutor(world, numel, [(b.start, b.tasks) for b in layout.buckets], dt, reduce_to_owner=rto,
+                            groups=groups)
+    ex.set_overlap(overlap)
+    probes = ex.flush_all(grads, probe=True)
+    om = oracle.owner_map(world, [(list(range(world)), tree.numel), (sub, ex_sizes)], rto)
+    assert np.array_equal(om["owner"], ex.omap.owner)
+    for i, b in enumerate(layout.buckets):
+        part = np.ascontiguousarray(host[:, b.start:b.start + b.size])
+        op = oracle.flush(world, part, b.tasks, om["owner"], full.n_params, None, code, True, rto)
+        host[:, b.start:b.start + b.size] = part
+        q = probes[i]
+        assert (q.tasks, q.reduced_elems, q.owner_elems, q.kept_elems) == \
+            (op["tasks"], op["reduced_elems"], op["owner_elems"], op["kept_elems"])
+    torch.cuda.synchronize()
+    got = to_bits(grads)
+    assert np.array_equal(got, host.view(np.uint16 if code == BF16 else np.uint32))
+    assert zc.device_status() == 0
+    assert ex._native is not None and zc.lib().dpred_executor_overlap_eligible(ex._native) == 1
+    with pytest.raises(zc.DpredError):
+        ex.flush_all_mapped(torch.empty(grads.shape, dtype=dt, pin_memory=True),
+                            [torch.empty(1, dtype=dt, pin_memory=True) for _ in range(world)], grads)
     ex.close()

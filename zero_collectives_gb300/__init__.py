@@ -726,6 +726,47 @@ class Zero1Executor:
         return self._finish(probes, probe)
 
 
+class InPlaceExecutor(Zero1Executor):
+    """The executor in place (dpred_executor_create with no destination
+    table): every flush writes its delivered results back into the gradient
+    rows themselves, row owner(t) for an owned parameter and every row for an
+    AllReduce one, as a bucket's collective does on the bucket's own memory.
+    The probes count what each row received.  A step is one native call with
+    launch overlap between buckets (in-place writes stay inside their own
+    bucket's columns); the host-buffer steps need destination buffers and are
+    not available."""
+
+    def __init__(self, world: int, numel, buckets, dtype, reduce_to_owner: bool = True, pre_div: bool = True,
+                 groups=None, probe_log: ProbeLog | None = None):
+        import torch
+        self.world = world
+        self.dtype = dtype
+        self.dt_code = BF16 if dtype == torch.bfloat16 else F32
+        self.reduce_to_owner, self.pre_div = reduce_to_owner, pre_div
+        groups = [(None, numel)] if groups is None else groups
+        self.omap = build_owner_map(world, groups, reduce_to_owner)
+        self.grad = None
+        self.buckets = [(int(s), np.ascontiguousarray(t, dtype=TASK_DTYPE)) for s, t in buckets]
+        self.sizes = [int((t["offset"] + t["numel"]).max()) if len(t) else 0 for _, t in self.buckets]
+        self.probe_log = probe_log
+        ws = max((flush_workspace_bytes(world, len(t)) for _, t in self.buckets), default=0)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device="cuda") if ws else None
+        self.overlap = True
+        self._native = None
+        self._bound = None
+
+    def _create(self, grads, ld, nb, starts, counts, tasks, ws_ptr, ws_bytes, handle):
+        if _dtype_code(grads) != self.dt_code:
+            raise TypeError("an in-place executor keeps the gradient dtype")
+        _check(lib().dpred_executor_create(self.world, _dtype_code(grads), self.dt_code, int(self.pre_div),
+                                           int(self.reduce_to_owner), self.omap.owner.ctypes.data, len(self.omap.owner),
+                                           grads.data_ptr(), ld, nb, starts.ctypes.data, counts.ctypes.data,
+                                           tasks.ctypes.data, None, ws_ptr, ws_bytes, ctypes.byref(handle)))
+
+    def _regions(self):
+        raise DpredError(-1, "host-buffer steps need destination buffers (in-place executor)")
+
+
 class PartitionedExecutor(Zero1Executor):
     """The executor over partitioned flushes (dpred_executor_create_partitioned):
     every rank receives exactly its own partition of the reduced gradients,

@@ -41,6 +41,7 @@ struct dpred_executor {
     bool overlap_ok = false;         // the device buckets share no byte
     bool mapped_overlap_ok = false;  // the mapped plans share no byte
     bool overlap_on = true;          // dpred_executor_set_overlap
+    bool in_place = false;           // results written back into the gradient rows
     void* workspace;
     size_t workspace_bytes;
     int64_t flushes = 0;
@@ -81,7 +82,7 @@ int setup_pipeline(dpred_executor* ex) {
 // Only then may consecutive flushes overlap on the GPU.
 bool buckets_independent(const std::vector<int64_t>& start, const std::vector<int64_t>& size,
                          const std::vector<std::vector<dpred::Dest>>& dests, int osz, const void* grads,
-                         int64_t grads_bytes) {
+                         int64_t grads_bytes, int64_t row_bytes, int isz) {
     std::vector<std::pair<int64_t, int64_t>> cols;
     for (size_t b = 0; b < start.size(); ++b)
         if (size[b] > 0) cols.emplace_back(start[b], start[b] + size[b]);
@@ -90,12 +91,21 @@ bool buckets_independent(const std::vector<int64_t>& start, const std::vector<in
         if (cols[i].first < cols[i - 1].second) return false;
     const uintptr_t g0 = reinterpret_cast<uintptr_t>(grads), g1 = g0 + (uintptr_t)grads_bytes;
     std::vector<std::pair<uintptr_t, uintptr_t>> r;
-    for (const auto& bd : dests)
-        for (const dpred::Dest& t : bd)
+    for (size_t b = 0; b < dests.size(); ++b)
+        for (const dpred::Dest& t : dests[b])
             if (t.numel > 0)
                 for (void* p : t.ptrs) {
                     const uintptr_t a = reinterpret_cast<uintptr_t>(p), e = a + (uintptr_t)(t.numel * osz);
-                    if (a < g1 && e > g0) return false;
+                    if (a < g1 && e > g0) {
+                        // in place: the range must lie inside one row, within this
+                        // bucket's own columns (which no other bucket reads or writes)
+                        if (osz != isz || row_bytes <= 0 || a < g0 || e > g1) return false;
+                        const uintptr_t off = a - g0;
+                        if (off % (uintptr_t)isz) return false;
+                        const int64_t col = (int64_t)((off % (uintptr_t)row_bytes) / (uintptr_t)isz);
+                        if (col < start[b] || col + t.numel > start[b] + size[b]) return false;
+                        continue;
+                    }
                     r.emplace_back(a, e);
                 }
     std::sort(r.begin(), r.end());
@@ -185,7 +195,8 @@ int add_bucket(dpred_executor* ex, int b, const dpred_task* bt, int nt, std::vec
 
 void finish_executor(dpred_executor* ex) {
     ex->overlap_ok = buckets_independent(ex->start, ex->size, ex->dests, esz(ex->out_dt), ex->grads,
-                                         (int64_t)ex->world * ex->ld * esz(ex->in_dt));
+                                         (int64_t)ex->world * ex->ld * esz(ex->in_dt), ex->ld * esz(ex->in_dt),
+                                         esz(ex->in_dt));
 }
 
 void release(dpred_executor* ex) {
@@ -230,18 +241,28 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
     int rc = new_executor(world, in_dtype, out_dtype, pre_div, grads, ld, n_buckets, bucket_start, bucket_tasks,
                           workspace, workspace_bytes, &ex);
     if (rc) return rc;
-    if (dst == nullptr && n_buckets > 0) {
+    ex->in_place = dst == nullptr;
+    if (ex->in_place && in_dtype != out_dtype) {
         delete ex;
-        return set_error(DPRED_E_INVAL, "the executor needs destination tables");
+        return set_error(DPRED_E_INVAL, "an in-place executor needs out_dtype == in_dtype");
     }
+    const int isz = esz(in_dtype);
     int64_t t0 = 0, d0 = 0;
     for (int b = 0; b < n_buckets; ++b) {
         const int nt = bucket_tasks[b];
         const dpred_task* bt = tasks + t0;
-        void* const* bd = dst + d0;
+        void* const* bd = ex->in_place ? nullptr : dst + d0;
         // Full validation through the public probe path (same rules as a flush).
         dpred_probe pr{};
         rc = dpred_flush_probe(world, bt, nt, owner, n_params, bd, reduce_to_owner, &pr);
+        if (rc == DPRED_OK && ex->in_place) {
+            std::vector<std::pair<int64_t, int64_t>> rg;
+            for (int t = 0; t < nt; ++t)
+                if (bt[t].numel > 0) rg.emplace_back(bt[t].offset, bt[t].offset + bt[t].numel);
+            std::sort(rg.begin(), rg.end());
+            for (size_t i = 1; i < rg.size() && rc == DPRED_OK; ++i)
+                if (rg[i].first < rg[i - 1].second) rc = set_error(DPRED_E_SIZE, "bucket %d: in-place tasks overlap", b);
+        }
         std::vector<Dest> plan(nt);
         for (int t = 0; t < nt && rc == DPRED_OK; ++t) {
             const int root = (reduce_to_owner && owner && owner[bt[t].param_id] >= 0) ? owner[bt[t].param_id] : -1;
@@ -249,7 +270,9 @@ int dpred_executor_create(int32_t world, int32_t in_dtype, int32_t out_dtype, in
             plan[t].numel = bt[t].numel;
             for (int r = 0; r < world; ++r) {
                 if (root >= 0 && r != root) continue;
-                void* p = bd[(int64_t)r * nt + t];
+                void* p = ex->in_place ? const_cast<char*>(static_cast<const char*>(grads)) +
+                                             ((int64_t)r * ld + bucket_start[b] + bt[t].offset) * isz
+                                       : bd[(int64_t)r * nt + t];
                 if (p) plan[t].ptrs.push_back(p);
             }
         }
@@ -342,6 +365,7 @@ int dpred_executor_flush_all_from_host(dpred_executor* ex, const void* host_grad
                                        dpred_probe* probes, void* stream) {
     using namespace dpred;
     if (!ex) return set_error(DPRED_E_INVAL, "null executor");
+    if (ex->in_place) return set_error(DPRED_E_INVAL, "host-buffer steps need destination buffers (in-place executor)");
     if (!host_grads || host_ld < 0) return set_error(DPRED_E_INVAL, "bad host gradients");
     if (n_regions < 0 || (n_regions > 0 && (!region_dev || !region_host || !region_bytes)))
         return set_error(DPRED_E_INVAL, "bad output regions");
@@ -405,6 +429,7 @@ int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, 
                                     dpred_probe* probes, void* stream) {
     using namespace dpred;
     if (!ex) return set_error(DPRED_E_INVAL, "null executor");
+    if (ex->in_place) return set_error(DPRED_E_INVAL, "host-buffer steps need destination buffers (in-place executor)");
     if (!host_grads || host_ld < 0) return set_error(DPRED_E_INVAL, "bad host gradients");
     if (reinterpret_cast<uintptr_t>(host_grads) % esz(ex->in_dt))
         return set_error(DPRED_E_ALIGN, "host gradients not aligned to their element size");
@@ -456,8 +481,10 @@ int dpred_executor_flush_all_mapped(dpred_executor* ex, const void* host_grads, 
             plans[b].ldg_only = true;
             mapped_dests.push_back(std::move(d));
         }
+        // (host-step destinations never lie inside the host gradient rows: row_bytes 0)
         ex->mapped_overlap_ok = buckets_independent(ex->start, ex->size, mapped_dests, osz, gdev,
-                                                    (int64_t)ex->world * host_ld * esz(ex->in_dt));
+                                                    (int64_t)ex->world * host_ld * esz(ex->in_dt), 0,
+                                                    esz(ex->in_dt));
         ex->mapped = std::move(plans);
         ex->mapped_key = std::move(key);
     }
