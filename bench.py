@@ -700,6 +700,12 @@ def rows(peak):
     ms_pm = timed(per_mb, 3, warm=1)
     out["accumulate_per_microbatch_step"] = entry(ms_pm, M * (4 * W * n + 4 * n) + 4 * n + (M - 1) * 12 * n,
                                                   workload="status quo: reduce every micro-batch", launches=2 * M)
+    # accumulator checkpoints (row f2): save reduces the W rows to the total a
+    # checkpoint holds; restore puts a total back as row 0 with the rest zero
+    ms_save = timed(lambda: zc.accumulator_save(acc, total), 5)
+    out["accumulator_save"] = entry(ms_save, 4 * W * n + 4 * n, workload="qwen3 W=4: W fp32 rows -> total")
+    ms_rest = timed(lambda: zc.accumulator_restore(acc, total), 5)
+    out["accumulator_restore"] = entry(ms_rest, 4 * n + 4 * W * n, workload="qwen3 W=4: total -> row 0, zeros elsewhere")
     del acc, gb, total, red, s_m
 
     # ReduceScatter / AllGather, M = 1 GiB bf16.
