@@ -163,7 +163,7 @@ struct FlushLaunch {
 
 // Vectors each thread keeps in flight per replica row: small world sizes take
 // several so that every SM still has enough bytes outstanding.
-inline int flush_batch(int world) { return world == 2 || world == 4 ? 2 : 1; }
+inline int flush_batch(int world) { return world == 2 || world == 3 || world == 4 ? 2 : 1; }
 
 // Work units of a plan task; vec_elems = input elements per 16-byte vector,
 // unit_vec = vectors per unit (kUnitVec x the batch).

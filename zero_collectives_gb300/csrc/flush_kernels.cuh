@@ -632,7 +632,7 @@ template <int W_T, int BATCH, typename Tin, typename Tout, typename Args>
 cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_only, bool write_heavy, bool pdl,
                           cudaStream_t s) {
     const int cap = flush_ctas_per_sm(W_T, write_heavy);
-    if constexpr (W_T > 0) {
+    if constexpr (W_T == 2 || W_T == 4 || W_T == 8 || W_T == 16) {  // the TMA form's world sizes
         if (!ldg_only && flush_path() == PATH_TMA) {  // auto: the register-streaming form measured faster on GB300
             auto k = flush_tma_kernel<W_T, Tin, Tout, Args>;
             constexpr size_t smem = tma_smem_bytes<W_T>();
@@ -691,6 +691,11 @@ int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
         case 4: return launch_flush_w<4, 2, Tin, Tout>(L, s);
         case 8: return launch_flush_w<8, 1, Tin, Tout>(L, s);
         case 16: return launch_flush_w<16, 1, Tin, Tout>(L, s);
+        // common world sizes that are not powers of two: the same unrolled
+        // body as above instead of the generic row loop
+        case 3: return launch_flush_w<3, 2, Tin, Tout>(L, s);
+        case 6: return launch_flush_w<6, 1, Tin, Tout>(L, s);
+        case 12: return launch_flush_w<12, 1, Tin, Tout>(L, s);
         default: return launch_flush_w<0, 1, Tin, Tout>(L, s);
     }
 }
