@@ -465,7 +465,8 @@ int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const v
  *   0 auto (the default: the family measured fastest on GB300 for each call:
  *     register streaming for the flush and ReduceScatter, TMA for AllGather),
  *   1 register streaming: every thread keeps one 16-byte load per replica row
- *     (flush) or per shard (AllGather) in flight and stores from registers,
+ *     (two at world 2, 3 and 4) for the flush, or per shard for AllGather, in
+ *     flight and stores from registers,
  *   2 TMA staging: the flush has one thread per SM stream 4 KB row tiles into a
  *     ring of shared-memory stages with cp.async.bulk (mbarrier-counted) while
  *     eight warps reduce from shared memory (world in {2, 4, 8, 16} only;
