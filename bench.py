@@ -347,6 +347,8 @@ def run_dpred(args):
         result["cpu_baseline_all_cores"] = cpu_baseline_all_cores(buckets, tree)
     if not args.no_rows:
         result["flush_paths"] = flush_path_ab(ex, grads, step_bytes, peak)
+        result["flush_bucket_calls_step"] = flush_bucket_calls(ex, grads, step_bytes, peak)
+        result["flush_bucket_per_call_overhead"] = per_call_overhead()
         del grads
         result["rows"] = rows(peak)
     if rank == 0:
@@ -541,6 +543,90 @@ def flush_path_ab(ex, grads, step_bytes, peak):
     return out
 
 
+def flush_bucket_calls(ex, grads, step_bytes, peak):
+    """The step as a caller of dpred_flush_bucket makes it: one call per bucket
+    (7 on the 402.8M W=8 workload), probe counters on, with and without the
+    overlap promise (consecutive buckets share no byte).  The executor's
+    prebuilt plans are not used; every call goes through the per-call entry
+    point (validation and planning are served by its plan cache after the
+    first step)."""
+    import zero_collectives_gb300 as zc
+    out = {}
+    calls = [(grads[:, s0:s0 + size], t, tab) for (s0, t), size, tab in zip(ex.buckets, ex.sizes, ex.tables)]
+    owner = ex.omap.owner
+    for overlap in (True, False):
+        def step():
+            for g, t, tab in calls:
+                zc.flush_bucket(g, t, owner, tab, zc.BF16, True, True, probe=True, overlap=overlap)
+        ms = timed(step, 20, warm=3)
+        gbs = step_bytes / (ms * 1e-3) / 1e9
+        out["overlap" if overlap else "no_overlap"] = {
+            "ms_per_step": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "calls_per_step": len(calls)}
+    return out
+
+
+def per_call_overhead():
+    """Host cost of one dpred_flush_bucket call on a small bucket (W=8, 16
+    tasks, 256 KB of gradients): host time per call over 2000 back-to-back
+    eager calls (perf_counter) through the Python binding and through a
+    pre-marshalled ctypes call, the first call (validation and planning) and
+    a repeated call (plan cache), and the device time per call measured with
+    CUDA events over the same loop."""
+    import ctypes
+    import time
+
+    import numpy as np
+    import torch
+
+    import zero_collectives_gb300 as zc
+    world, n_tasks, per = 8, 16, 1024
+    grads = torch.randn((world, n_tasks * per), device="cuda").to(torch.bfloat16)
+    tasks = np.zeros(n_tasks, dtype=zc.TASK_DTYPE)
+    tasks["param_id"] = np.arange(n_tasks)
+    tasks["offset"] = np.arange(n_tasks) * per
+    tasks["numel"] = per
+    owner = (np.arange(n_tasks) % world).astype(np.int32)
+    bufs = [torch.empty(per, dtype=torch.bfloat16, device="cuda") for _ in range(n_tasks)]
+    dst = zc.DstTable(world, n_tasks, [bufs[t].data_ptr() if owner[t] == r else 0
+                                       for r in range(world) for t in range(n_tasks)])
+    s = torch.cuda.current_stream()
+    L = zc.lib()
+    probe = zc._Probe()
+    args = (world, zc.BF16, grads.data_ptr(), grads.stride(0), tasks.ctypes.data, n_tasks, owner.ctypes.data,
+            n_tasks, zc.BF16, dst.c, 1, 1, 0, ctypes.byref(probe), None, 0, s.cuda_stream)
+    out = {"bucket": f"W={world}, {n_tasks} tasks x {per} bf16 elements ({world * n_tasks * per * 2} bytes read)"}
+    for name, fn in (("python_binding", lambda: zc.flush_bucket(grads, tasks, owner, dst, probe=True)),
+                     ("ctypes_premarshalled", lambda: L.dpred_flush_bucket(*args))):
+        for _ in range(50):
+            fn()
+        torch.cuda.synchronize()
+        a, b = events(2)
+        n = 2000
+        a.record(s)
+        t0 = time.perf_counter()
+        for _ in range(n):
+            fn()
+        host_us = (time.perf_counter() - t0) / n * 1e6
+        b.record(s)
+        torch.cuda.synchronize()
+        out[name] = {"host_us_per_call": round(host_us, 2), "device_us_per_call": round(a.elapsed_time(b) / n * 1e3, 2)}
+    # first call of a new table (validation and planning) against a repeated one
+    tasks2 = tasks.copy()
+    firsts = []
+    for k in range(20):
+        tasks2["numel"] = per - 1 - k  # a new table every time: a plan-cache miss
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        L.dpred_flush_bucket(world, zc.BF16, grads.data_ptr(), grads.stride(0), tasks2.ctypes.data, n_tasks,
+                             owner.ctypes.data, n_tasks, zc.BF16, dst.c, 1, 1, 0, ctypes.byref(probe), None, 0,
+                             s.cuda_stream)
+        firsts.append((time.perf_counter() - t0) * 1e6)
+    torch.cuda.synchronize()
+    out["ctypes_first_call_us_median"] = round(float(np.median(firsts)), 2)
+    return out
+
+
 # -------------------------------------------------------- other hot rows ---
 
 def timed(fn, reps, warm=2):
@@ -708,8 +794,34 @@ def rows(peak):
     out["accumulator_restore"] = entry(ms_rest, 4 * n + 4 * W * n, workload="qwen3 W=4: total -> row 0, zeros elsewhere")
     del acc, gb, total, red, s_m
 
-    # ReduceScatter / AllGather, M = 1 GiB bf16.
+    # HBM ceilings measured by kernels that do nothing else (no AllGather
+    # involved): a write-only fill (the best of 16-byte, 32-byte and bulk
+    # stores over 4 GiB) and, for the AllGather's own mix of reads and writes
+    # (M read, N*M written), a stream of exactly that mix in which no store
+    # waits for a load.
+    wbuf = torch.empty(4 << 30, dtype=torch.uint8, device="cuda")
+    fills = {}
+    for method in (0, 1, 2):
+        fills[method] = timed(lambda: zc.fill_pattern(wbuf, 0x3F803F80, method, 0 if method < 2 else 1), 10)
+    best = min(fills, key=fills.get)
+    out["hbm_write_ceiling"] = entry(fills[best], 4 << 30, workload="write-only fill of 4 GiB (dpred_fill_pattern)",
+                                     method=best, ms_by_method={m: round(v, 4) for m, v in fills.items()})
+    write_gbs = out["hbm_write_ceiling"]["GB/s"]
+    ms = timed(lambda: wbuf.zero_(), 10)
+    out["torch_zero_fill_4GiB"] = entry(ms, 4 << 30, workload="write-only reference (torch zero_)")
+    del wbuf
     Mel = 1 << 29
+    mixed_ms = {}
+    src = torch.empty(Mel, dtype=torch.bfloat16, device="cuda")
+    for N in (8, 4):
+        dstm = torch.empty(N * Mel, dtype=torch.bfloat16, device="cuda")
+        mixed_ms[N] = timed(lambda: zc.stream_mixed(src, dstm), 10)
+        out[f"hbm_mixed_ceiling_1r{N}w"] = entry(mixed_ms[N], Mel * 2 + N * Mel * 2,
+                                                 workload=f"1 GiB read + {N} GiB written, no dependency (dpred_stream_mixed)")
+        del dstm
+    del src
+
+    # ReduceScatter / AllGather, M = 1 GiB bf16.
     for N in (8, 4):
         S = Mel // N
         x = torch.empty((N, Mel), dtype=torch.bfloat16, device="cuda")
@@ -723,38 +835,22 @@ def rows(peak):
         out[f"reduce_scatter_N{N}_tma"] = entry(ms, N * Mel * 2 + Mel * 2, workload=f"N={N}, M=1 GiB bf16, TMA path")
         del x
         ag = torch.empty((N, Mel), dtype=torch.bfloat16, device="cuda")
+        model_ms = (N * Mel * 2 / (write_gbs * 1e9) + Mel * 2 / (peak * 1e9)) * 1e3
         for order, name in ((0, "canonical"), (1, "ring")):
-            ms = timed(lambda: zc.allgather(rs, ag, order), 10)
-            out[f"allgather_{name}_N{N}"] = entry(ms, Mel * 2 + N * Mel * 2, workload=f"N={N}, M=1 GiB bf16 (TMA form)")
-            prev = zc.set_flush_path(zc.PATH_LDG)
-            ms = timed(lambda: zc.allgather(rs, ag, order), 10)
-            zc.set_flush_path(prev)
-            out[f"allgather_{name}_N{N}_ldg"] = entry(ms, Mel * 2 + N * Mel * 2,
-                                                      workload=f"N={N}, M=1 GiB bf16, register-streaming form")
-        wr = torch.empty(N * Mel, dtype=torch.bfloat16, device="cuda")
-        ms = timed(lambda: wr.zero_(), 10)
-        out[f"torch_zero_fill_{N}GiB"] = entry(ms, N * Mel * 2, workload="write-only reference (torch zero_)")
-        del wr
+            for form, suffix, what in ((zc.AG_AUTO, "", "default form"), (zc.AG_TMA1, "_tma1", "bulk copies, unskewed"),
+                                       (zc.AG_REGISTER, "_ldg", "register-streaming form")):
+                prev = zc.set_allgather_form(form)
+                ms = timed(lambda: zc.allgather(rs, ag, order), 10)
+                zc.set_allgather_form(prev)
+                r = entry(ms, Mel * 2 + N * Mel * 2, workload=f"N={N}, M=1 GiB bf16, {what}")
+                r["frac_of_write_model"] = round(model_ms / ms, 4)
+                r["frac_of_mixed_ceiling"] = round(mixed_ms[N] / ms, 4)
+                out[f"allgather_{name}_N{N}{suffix}"] = r
         del ag, rs
-    # HBM write ceiling, measured by the same TMA AllGather with N=64: 16 GiB of
-    # stores against 256 MiB of loads (98.5% writes).  The N=8 and N=4 rows
-    # are then compared with the time that ceiling plus the copy peak for the
-    # loads predicts.
-    N, S = 64, 1 << 21
-    x = torch.empty((N, S), dtype=torch.bfloat16, device="cuda")
-    datagen.fill_device(x.data_ptr(), N, S, S, BF16, UNIFORM, 5, 0, 1, 0, 1.0, s)
-    ag = torch.empty((N, N * S), dtype=torch.bfloat16, device="cuda")
-    ms = timed(lambda: zc.allgather(x, ag, 0), 5)
-    w64 = N * N * S * 2
-    write_gbs = w64 / (ms * 1e-3) / 1e9
-    out["allgather_N64_write_ceiling"] = entry(ms, w64 + N * S * 2, workload="N=64, 4 MiB shards: 16 GiB written")
-    out["allgather_N64_write_ceiling"]["write_GBps"] = round(write_gbs, 1)
-    del x, ag
-    for N in (8, 4):
-        for name in ("canonical", "ring"):
-            r = out[f"allgather_{name}_N{N}"]
-            model_ms = (N * Mel * 2 / (write_gbs * 1e9) + Mel * 2 / (peak * 1e9)) * 1e3
-            r["frac_of_write_model"] = round(model_ms / r["ms"], 4)
+    # the restore writes W rows for one read (1 read : 4 writes at W=4): the
+    # N=4 mixed stream has the same mix
+    out["accumulator_restore"]["frac_of_mixed_ceiling"] = round(
+        out["accumulator_restore"]["GB/s"] / out["hbm_mixed_ceiling_1r4w"]["GB/s"], 4)
     out["allgather_schedules_N8"] = schedule_fit(8, Mel)
     torch.cuda.empty_cache()
     return out

@@ -198,27 +198,45 @@ size_t dpred_flush_workspace_bytes(int32_t world, int32_t n_tasks);
  *    delivered rows of grads.  out_dtype must equal in_dtype and tasks must
  *    not overlap.
  * owner: host [n_params] or NULL (no owners: AllReduce everything, the
- * flag-off path).  pre_div != 0 divides every term by world.  checked != 0
- * additionally verifies that an owner task has no non-NULL destination on a
- * rank other than its owner (DPRED_E_MISMATCH).  probe (host, may be NULL)
- * receives the counters of dpred_flush_probe.  workspace (device, may be NULL
- * when dpred_flush_workspace_bytes() is 0) of workspace_bytes bytes.
+ * flag-off path).  pre_div != 0 divides every term by world.  flags (an OR
+ * of the DPRED_FLUSH_* bits below, 0 for none):
+ *  - DPRED_FLUSH_CHECKED additionally verifies that an owner task has no
+ *    non-NULL destination on a rank other than its owner (DPRED_E_MISMATCH);
+ *  - DPRED_FLUSH_OVERLAP is the caller's promise that this flush shares no
+ *    byte with the work enqueued on `stream` just before it (normally the
+ *    previous bucket's flush): neither reads what that work writes nor
+ *    writes what it reads or writes.  The flush may then start on the SMs
+ *    that the previous flush's last wave leaves idle (programmatic dependent
+ *    launch); it still completes after that flush, so the stream's order of
+ *    completion is unchanged.  Plans that do not fit inside the launch
+ *    (dpred_flush_workspace_bytes() > 0) ignore the bit.  A promise that
+ *    does not hold makes the results undefined.
+ * probe (host, may be NULL) receives the counters of dpred_flush_probe.
+ * workspace (device, may be NULL when dpred_flush_workspace_bytes() is 0) of
+ * workspace_bytes bytes.
+ * Repeated calls: each thread keeps the validated plans and counters of its
+ * 16 most recent distinct calls, keyed on every input byte (scalars, the task
+ * table, owner[param_id] of each task and the destination table); a call
+ * whose inputs equal one of them skips validation and planning.  Pointer
+ * values are compared, never the memory behind them.
  * Asynchronous on `stream`; grads, dst buffers and workspace must stay valid
- * until the work completes.  Errors: DPRED_E_INVAL, DPRED_E_ALIGN,
- * DPRED_E_SIZE (a task outside [0, ld), overlapping in-place tasks, workspace
- * too small), DPRED_E_MISMATCH, DPRED_E_CUDA.
+ * until the work completes.  Errors: DPRED_E_INVAL (including unknown flag
+ * bits), DPRED_E_ALIGN, DPRED_E_SIZE (a task outside [0, ld), overlapping
+ * in-place tasks, workspace too small), DPRED_E_MISMATCH, DPRED_E_CUDA.
  */
+#define DPRED_FLUSH_CHECKED 1
+#define DPRED_FLUSH_OVERLAP 2
 int dpred_flush_bucket(int32_t world, int32_t in_dtype, void* grads, int64_t ld, const dpred_task* tasks,
                        int32_t n_tasks, const int32_t* owner, int32_t n_params, int32_t out_dtype, void* const* dst,
-                       int32_t pre_div, int32_t reduce_to_owner, int32_t checked, dpred_probe* probe,
+                       int32_t pre_div, int32_t reduce_to_owner, int32_t flags, dpred_probe* probe,
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Allocation-free bucket flush.  The pages have no counterpart to this entry
- * point; it serves callers that cannot allocate device memory: code that
- * runs while a CUDA graph is being captured, runtimes that carve all device
- * memory out of a fixed budget up front, and plug-ins that live inside
- * another framework's allocator.
+ * point; it serves callers that cannot allocate device memory: runtimes that
+ * carve all device memory out of a fixed budget up front and have none left
+ * to lend, and plug-ins that live inside another framework's allocator and
+ * may not allocate device memory of their own.
  *
  * Same arguments and results as dpred_flush_bucket, minus the workspace.  A
  * bucket whose task table does not fit inside the launch uses a scratch
@@ -238,7 +256,7 @@ int dpred_flush_bucket(int32_t world, int32_t in_dtype, void* grads, int64_t ld,
 #define DPRED_NOALLOC_SCRATCH_BYTES (1u << 20)
 int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int64_t ld, const dpred_task* tasks,
                                int32_t n_tasks, const int32_t* owner, int32_t n_params, int32_t out_dtype,
-                               void* const* dst, int32_t pre_div, int32_t reduce_to_owner, int32_t checked,
+                               void* const* dst, int32_t pre_div, int32_t reduce_to_owner, int32_t flags,
                                dpred_probe* probe, void* stream);
 
 /*
@@ -479,6 +497,29 @@ int dpred_allgather(int32_t n_nodes, int64_t shard_elems, int32_t dtype, const v
 int dpred_set_flush_path(int32_t path);
 
 /*
+ * Kernel form of later dpred_allgather calls in this process (a tuning knob;
+ * every form writes the same bytes):
+ *   0 auto: form 1 when dpred_set_flush_path selected register streaming,
+ *     else form 5,
+ *   1 register streaming (16-byte loads and streaming stores, shard by shard),
+ *   2 bulk copies, one issuing thread per SM: 16 KB shard tiles bulk-loaded
+ *     into an 8-stage shared-memory ring and bulk-stored to the N rows,
+ *   3 bulk copies, four issuing warps per SM, each with its own 6-stage ring
+ *     of 8 KB tiles and its own bulk group,
+ *   4 staged warp stores: one thread bulk-loads 16 KB tiles into an 8-stage
+ *     ring, eight warps store each tile to the N rows with 16-byte streaming
+ *     stores,
+ *   5 bulk copies with rows skewed in time: one issuing thread per SM keeps
+ *     the last min(N, 8) tiles staged (16 KB tiles, 12 stages) and in each
+ *     step stores tile q - (i mod 8) to row i, so that concurrent stores to
+ *     neighbouring rows are not a whole row apart,
+ *   6 form 5 with 8 KB tiles and 20 stages.
+ * Forms 2-6 need 16-byte aligned rows (else form 1 runs).  Returns the
+ * previous form, or DPRED_E_INVAL.  Not thread-safe against concurrent calls.
+ */
+int dpred_set_allgather_form(int32_t form);
+
+/*
  * AllGather schedules, executed step by step.  [AG] "Ring AllGather" (N-1
  * steps; in step s every node forwards to its right neighbour the chunk it
  * received in step s-1), the bidirectional ring (eq. ag-bidir-ring:
@@ -508,6 +549,36 @@ int dpred_allgather_schedule_init(int32_t schedule, int32_t n_nodes, int64_t sha
                                   const void* in, void* bufs, void* stream);
 int dpred_allgather_schedule_step(int32_t schedule, int32_t n_nodes, int64_t shard_elems, int32_t dtype, void* bufs,
                                   int32_t step, void* stream);
+
+/*
+ * Write-only fill (no counterpart in the pages; a measuring aid): writes the
+ * 32-bit pattern over bytes of dst (device) and reads nothing, so its rate is
+ * the device's HBM write ceiling, the bound of store-dominated kernels such
+ * as the AllGather ([AG] "理论下界": its cost is the N·M output).
+ *   method 0: 16-byte streaming stores from every thread of a persistent grid
+ *             (dst and bytes multiples of 16),
+ *   method 1: 32-byte streaming stores (dst and bytes multiples of 32),
+ *   method 2: bulk copies (cp.async.bulk) of a 16 KB shared-memory tile by
+ *             four issuing warps per CTA (dst and bytes multiples of 16).
+ * ctas_per_sm: CTAs per SM of the persistent grid (0 = as many as fit;
+ * method 2 takes 0 as 1).  Errors: DPRED_E_INVAL, DPRED_E_ALIGN,
+ * DPRED_E_CUDA.  Asynchronous on `stream`.
+ */
+int dpred_fill_pattern(void* dst, size_t bytes, uint32_t pattern, int32_t method, int32_t ctas_per_sm,
+                       void* stream);
+
+/*
+ * Mixed streaming (no counterpart in the pages; a measuring aid): bulk-loads
+ * read_bytes of src (device) into shared memory that nothing reads, and
+ * bulk-stores a constant pattern over write_bytes of dst (device), the loads
+ * spread evenly between the stores.  No store depends on a load, so the rate
+ * is what HBM sustains for this mix of reads and writes -- the ceiling of a
+ * kernel with the same mix, e.g. the AllGather (reads M, writes N·M).
+ * Buffers and sizes must be multiples of 16 bytes (DPRED_E_ALIGN).  A bounded
+ * wait that gives up records DPRED_E_TIMEOUT in the device error word.
+ * Errors: DPRED_E_INVAL, DPRED_E_ALIGN, DPRED_E_CUDA.  Asynchronous on `stream`.
+ */
+int dpred_stream_mixed(const void* src, size_t read_bytes, void* dst, size_t write_bytes, void* stream);
 
 /*
  * Device error word: 0, or the DPRED_E_* code of the first device-side

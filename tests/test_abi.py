@@ -178,6 +178,11 @@ def test_empty_calls_are_no_ops(L):
     # zero tasks / zero elements enqueue nothing and succeed without a GPU
     t = np.zeros(0, dtype=zc.TASK_DTYPE)
     assert L.dpred_flush_bucket(4, 0, None, 0, t.ctypes.data, 0, None, 0, 0, None, 1, 1, 0, None, None, 0, None) == 0
+    # the same call again (served by the plan cache), and with the overlap promise
+    assert L.dpred_flush_bucket(4, 0, None, 0, t.ctypes.data, 0, None, 0, 0, None, 1, 1, 0, None, None, 0, None) == 0
+    assert L.dpred_flush_bucket(4, 0, None, 0, t.ctypes.data, 0, None, 0, 0, None, 1, 1, 3, None, None, 0, None) == 0
+    # unknown flag bits are rejected
+    assert L.dpred_flush_bucket(4, 0, None, 0, t.ctypes.data, 0, None, 0, 0, None, 1, 1, 4, None, None, 0, None) == -1
     assert L.dpred_flush_workspace_bytes(8, 64) == 0          # 512 destinations at most: inline
     assert L.dpred_flush_workspace_bytes(8, 100) == 100 * 32 + 8 * 100 * 8
     assert L.dpred_flush_workspace_bytes(2, 200) == 200 * 32 + 2 * 200 * 8
@@ -283,6 +288,22 @@ def test_in_place_executor_without_a_gpu(L):
 def test_flush_path_and_pipeline_argument_errors(L):
     with pytest.raises(zc.DpredError):
         zc.set_flush_path(7)
+    with pytest.raises(zc.DpredError):
+        zc.set_allgather_form(7)
+    prev = zc.set_allgather_form(zc.AG_STAGED)
+    assert zc.set_allgather_form(prev) == zc.AG_STAGED
+    # the write-only fill rejects bad arguments before any launch
+    assert L.dpred_fill_pattern(0x200000, 64, 0, 3, 0, None) == -1             # unknown method
+    assert L.dpred_fill_pattern(None, 64, 0, 0, 0, None) == -1                 # null destination
+    assert L.dpred_fill_pattern(0x200008, 64, 0, 0, 0, None) == -2             # not 16-byte aligned
+    assert L.dpred_fill_pattern(0x200010, 64, 0, 1, 0, None) == -2             # not 32-byte aligned
+    assert L.dpred_fill_pattern(0x200000, 48, 0, 1, 0, None) == -2             # size not a multiple of 32
+    assert L.dpred_fill_pattern(0x200000, 64, 0, 0, 33, None) == -1            # too many CTAs per SM
+    assert L.dpred_fill_pattern(None, 0, 0, 0, 0, None) == 0                   # nothing to write
+    assert L.dpred_stream_mixed(None, 0, None, 0, None) == 0                   # nothing to move
+    assert L.dpred_stream_mixed(None, 16, 0x200000, 16, None) == -1            # null source
+    assert L.dpred_stream_mixed(0x200000, 16, 0x300008, 16, None) == -2        # unaligned destination
+    assert L.dpred_stream_mixed(0x200000, 24, 0x300000, 16, None) == -2        # size not a multiple of 16
     prev = zc.set_flush_path(zc.PATH_LDG)
     assert zc.set_flush_path(prev) == zc.PATH_LDG
     # the host pipeline rejects bad arguments before touching any stream

@@ -1,8 +1,8 @@
 """The allocation-free flush entry point (dpred_flush_bucket_noalloc).
 
-It exists for callers that cannot allocate device memory -- code running
-under CUDA graph capture, runtimes working inside a fixed device budget,
-plug-ins living inside another framework's allocator.  Instead of a caller
+It exists for callers that cannot allocate device memory -- runtimes working
+inside a fixed device budget, plug-ins living inside another framework's
+allocator.  Instead of a caller
 workspace it keeps large task tables in a 1 MiB scratch array compiled into
 the library.  These tests call it through the C ABI and compare its output
 with the regular dpred_flush_bucket (given a workspace) on the same inputs,

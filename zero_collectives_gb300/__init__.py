@@ -100,6 +100,9 @@ def lib() -> ctypes.CDLL:
         L.dpred_allgather.argtypes = [i32, i64, i32, vp, vp, i32, vp]
         L.dpred_device_status.argtypes = [vp, i32]
         L.dpred_set_flush_path.argtypes = [i32]
+        L.dpred_set_allgather_form.argtypes = [i32]
+        L.dpred_fill_pattern.argtypes = [vp, ctypes.c_size_t, ctypes.c_uint32, i32, i32, vp]
+        L.dpred_stream_mixed.argtypes = [vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
         L.dpred_selftest_wait_timeout.argtypes = [i64, vp]
         L.dpred_selftest_bounds.argtypes = [vp]
         L.dpred_host_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
@@ -285,12 +288,17 @@ def flush_workspace_bytes(world: int, n_tasks: int) -> int:
     return int(lib().dpred_flush_workspace_bytes(world, n_tasks))
 
 
+FLUSH_CHECKED, FLUSH_OVERLAP = 1, 2
+
+
 def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
                  pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False, probe: bool = False,
-                 flush_index: int = 0, workspace=None, stream=None):
+                 flush_index: int = 0, workspace=None, stream=None, overlap: bool = False):
     """grads: CUDA tensor [W, m] (row stride = ld, e.g. a column slice of the
     whole [W, n] gradient); tasks: TASK_DTYPE array; owner: int32 per param or
-    None; dst: DstTable or None (in place).  Returns a Probe when probe=True."""
+    None; dst: DstTable or None (in place).  overlap=True promises that this
+    flush shares no byte with the work just before it on the stream
+    (DPRED_FLUSH_OVERLAP).  Returns a Probe when probe=True."""
     if grads.dim() != 2 or grads.stride(1) != 1:
         raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
     world = grads.shape[0]
@@ -304,10 +312,11 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
         p.flush_index = flush_index
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
                                                              workspace.numel() * workspace.element_size())
+    flags = (FLUSH_CHECKED if checked else 0) | (FLUSH_OVERLAP if overlap else 0)
     _check(lib().dpred_flush_bucket(world, in_dt, grads.data_ptr(), ld, t.ctypes.data, len(t),
                                     None if own is None else own.ctypes.data, 0 if own is None else len(own),
                                     out_dt, None if dst is None else dst.c, int(pre_div), int(reduce_to_owner),
-                                    int(checked), None if p is None else ctypes.byref(p), ws_ptr, ws_bytes,
+                                    flags, None if p is None else ctypes.byref(p), ws_ptr, ws_bytes,
                                     _stream(stream)))
     return _probe_from(p, world) if p is not None else None
 
@@ -315,10 +324,11 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
 def flush_bucket_noalloc(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
                          pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False,
                          probe: bool = False, flush_index: int = 0, stream=None):
-    """flush_bucket for callers that cannot allocate device memory (e.g. under
-    CUDA graph capture or inside a fixed device budget): no workspace, the
-    library's own 1 MiB scratch holds large task tables.  Calls that overlap on
-    the GPU share that scratch, so issue them on one stream."""
+    """flush_bucket for callers that cannot allocate device memory (a runtime
+    with a fixed device budget, a plug-in inside another framework's
+    allocator): no workspace, the library's own 1 MiB scratch holds large task
+    tables.  Calls that overlap on the GPU share that scratch, so issue them
+    on one stream."""
     if grads.dim() != 2 or grads.stride(1) != 1:
         raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
     world = grads.shape[0]
@@ -453,6 +463,32 @@ def set_flush_path(path: int) -> int:
     if rc < 0:
         _check(rc)
     return rc
+
+
+AG_AUTO, AG_REGISTER, AG_TMA1, AG_TMA4, AG_STAGED, AG_SKEW, AG_SKEW8K = 0, 1, 2, 3, 4, 5, 6
+
+
+def set_allgather_form(form: int) -> int:
+    """Kernel form of later AllGathers (AG_*, see dpred_set_allgather_form).  Returns the previous one."""
+    rc = lib().dpred_set_allgather_form(int(form))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def fill_pattern(t, pattern: int = 0, method: int = 0, ctas_per_sm: int = 0, stream=None):
+    """Write-only fill of a CUDA tensor's bytes (dpred_fill_pattern: the HBM write ceiling)."""
+    _check(lib().dpred_fill_pattern(t.data_ptr(), t.numel() * t.element_size(), int(pattern) & 0xFFFFFFFF,
+                                    int(method), int(ctas_per_sm), _stream(stream)))
+    return t
+
+
+def stream_mixed(src, dst, read_bytes: int | None = None, write_bytes: int | None = None, stream=None):
+    """Read src and write dst concurrently with no dependency (dpred_stream_mixed:
+    the HBM ceiling for that mix of reads and writes)."""
+    rb = src.numel() * src.element_size() if read_bytes is None else int(read_bytes)
+    wb = dst.numel() * dst.element_size() if write_bytes is None else int(write_bytes)
+    _check(lib().dpred_stream_mixed(src.data_ptr(), rb, dst.data_ptr(), wb, _stream(stream)))
 
 
 def selftest_wait_timeout(budget_cycles: int = 2_000_000, stream=None) -> None:

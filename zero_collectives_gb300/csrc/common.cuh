@@ -216,6 +216,11 @@ int launch_accumulator_restore(int world, int64_t n, float* acc, const float* to
 
 int launch_allgather(int n_nodes, int64_t shard_elems, int esize, const void* in, void* out, int order,
                      cudaStream_t s);
+// AllGather kernel form (see dpred_set_allgather_form); set_allgather_form
+// returns the previous form, or -1 for an unknown one.
+enum AllGatherForm : int { AG_AUTO = 0, AG_REGISTER = 1, AG_TMA1 = 2, AG_TMA4 = 3, AG_STAGED = 4, AG_SKEW = 5, AG_SKEW8K = 6 };
+int allgather_form();
+int set_allgather_form(int form);
 
 // Plan-driven byte copy (the relayout pass): triples of {src byte offset, dst byte offset, bytes}.
 int launch_copy_plan(const char* src, char* dst, const std::vector<int64_t>& triples, void* workspace,

@@ -2,12 +2,12 @@
 // cannot allocate device memory.
 //
 // dpred_flush_bucket keeps a large bucket's task table in a device workspace
-// that the caller passes in.  Some callers cannot produce one: code that runs
-// while a CUDA graph is being captured (cudaMalloc is not allowed there),
-// runtimes that hand out all device memory up front from a fixed budget, and
-// plug-ins that run inside another framework's allocator and must not touch
-// device memory of their own.  For them this entry point uses a fixed scratch
-// array that lives in the library itself instead of a caller workspace.
+// that the caller passes in.  Some callers cannot produce one: runtimes that
+// hand out all device memory up front from a fixed budget and have nothing
+// left to lend, and plug-ins that run inside another framework's allocator
+// and may not allocate device memory of their own.  For them this entry point
+// uses a fixed scratch array that lives in the library itself instead of a
+// caller workspace.
 //
 // The scratch array is a file-scope __device__ variable, so every GPU that
 // loads the library holds its kScratchBytes until the process exits.  Host
@@ -52,7 +52,7 @@ int scratch_address(void** out) {
 extern "C" int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void* grads, int64_t ld,
                                           const dpred_task* tasks, int32_t n_tasks, const int32_t* owner,
                                           int32_t n_params, int32_t out_dtype, void* const* dst, int32_t pre_div,
-                                          int32_t reduce_to_owner, int32_t checked, dpred_probe* probe,
+                                          int32_t reduce_to_owner, int32_t flags, dpred_probe* probe,
                                           void* stream) {
     if (world < 1 || world > DPRED_MAX_WORLD)
         return dpred::set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
@@ -67,5 +67,5 @@ extern "C" int dpred_flush_bucket_noalloc(int32_t world, int32_t in_dtype, void*
     int rc = scratch_address(&scratch);
     if (rc != DPRED_OK) return rc;
     return dpred_flush_bucket(world, in_dtype, grads, ld, tasks, n_tasks, owner, n_params, out_dtype, dst, pre_div,
-                              reduce_to_owner, checked, probe, scratch, kScratchBytes, stream);
+                              reduce_to_owner, flags, probe, scratch, kScratchBytes, stream);
 }
