@@ -32,7 +32,7 @@ METRIC = "bucket-flush achieved HBM GB/s and % of GB300 peak; grad-elems/s at W=
 WORKLOAD = "zero1-bucket-flush 402.8M params W=8 bf16 reduce-to-owner (7 buckets of <=52,428,800 elems)"
 FALLBACK_HBM_GBS = 6800.0
 SEED, SIGMA, WORLD = 3, 1e-3, 8
-KERNEL_SOURCES = ["flush_kernels.cuh", "flush_bf16.cu", "common.cuh"]
+KERNEL_SOURCES = ["flush_kernels.cuh", "flush_w8.cu", "common.cuh"]
 
 
 def parse():
@@ -53,6 +53,8 @@ def parse():
                     help="flush sweep: bucket sizes 1 KB-1 GB per replica, W in {2,4,8,16}, bf16/fp32, eager and "
                          "CUDA-graph replay; one JSON line per case")
     ap.add_argument("--sweep-worlds", default="2,4,8,16", help="--sweep: world sizes to run (comma-separated)")
+    ap.add_argument("--sweep-kb", default="1,16,256,4096,65536,1048576",
+                    help="--sweep: bucket sizes per replica row in KB (comma-separated)")
     ap.add_argument("--row", choices=["allgather", "reduce_scatter", "accumulate"], default=None,
                     help="time one other hot-path row alone (small profiling cases) and print its JSON line")
     ap.add_argument("--row-nodes", type=int, default=8)
@@ -1049,7 +1051,7 @@ def sweep(args):
     for W in [int(w) for w in args.sweep_worlds.split(",")]:
         for dt, code in ((torch.bfloat16, BF16), (torch.float32, F32)):
             esize = 2 if code == BF16 else 4
-            for kb in (1, 16, 256, 4096, 65536, 1048576):
+            for kb in [int(k) for k in args.sweep_kb.split(",")]:
                 elems = max(kb * 1024 // esize, 64 * W)
                 tree = workloads.straddle_tree(W, elems, W - 1, pieces=2)
                 ex_sizes = np.array([96, 64, 32], np.int64)
@@ -1079,6 +1081,18 @@ def sweep(args):
                     for e, g in zip(exs, gs):
                         e.flush_all(g)
 
+                # the same flushes as direct dpred_flush_bucket calls (plan cache
+                # after the first), with and without the overlap promise (the
+                # copies share no byte)
+                calls = []
+                for e, g in zip(exs, gs):
+                    for (s0, t), size, tab in zip(e.buckets, e.sizes, e.tables):
+                        calls.append((g[:, s0:s0 + size], t, tab, e.omap.owner))
+
+                def per_call(overlap):
+                    for g, t, tab, own in calls:
+                        zc.flush_bucket(g, t, own, tab, code, True, True, overlap=overlap)
+
                 side = torch.cuda.Stream()
                 graph = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(graph, stream=side):
@@ -1087,6 +1101,8 @@ def sweep(args):
                 clocks.start()
                 ms_e = timed(eager, reps // copies, warm=3) / copies
                 ms_g = timed(graph.replay, reps // copies, warm=3) / copies
+                ms_c = timed(lambda: per_call(False), reps // copies, warm=3) / copies
+                ms_o = timed(lambda: per_call(True), reps // copies, warm=3) / copies
                 clk = clocks.stop()
                 line = {"sweep": True, "world": W, "dtype": "bf16" if code == BF16 else "f32",
                         "bucket_bytes_per_replica": full.total * esize, "elems": full.total, "copies": copies,
@@ -1094,6 +1110,11 @@ def sweep(args):
                         "eager_GBps": round(nbytes / (ms_e * 1e-3) / 1e9, 1),
                         "graph_GBps": round(nbytes / (ms_g * 1e-3) / 1e9, 1),
                         "graph_frac_of_peak": round(nbytes / (ms_g * 1e-3) / 1e9 / peak, 4),
+                        "eager_frac_of_peak": round(nbytes / (ms_e * 1e-3) / 1e9 / peak, 4),
+                        "per_call_us": round(ms_c * 1e3, 2),
+                        "per_call_frac_of_peak": round(nbytes / (ms_c * 1e-3) / 1e9 / peak, 4),
+                        "per_call_overlap_us": round(ms_o * 1e3, 2),
+                        "per_call_overlap_frac_of_peak": round(nbytes / (ms_o * 1e-3) / 1e9 / peak, 4),
                         "sm_mhz": clk["sm_mhz"], "mem_mhz_min": clk["mem_mhz_min"], "clock_reasons": clk["reasons"]}
                 print(json.dumps(line), flush=True)
                 for e in exs:

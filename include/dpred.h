@@ -616,6 +616,20 @@ int dpred_selftest_wait_timeout(int64_t budget_cycles, void* stream);
  */
 int dpred_selftest_bounds(void* stream);
 
+/*
+ * Self-test of the flush's pre-division (no counterpart in the pages): for
+ * every fp32 bit pattern x (2^32 inputs), and again for every bf16 value,
+ * compares the quotient the flush kernels' vector paths use for a rank count
+ * of `world` -- a multiply by the exact reciprocal for powers of two; for
+ * other counts the division-free forms (Markstein's correction for fp32
+ * terms, a split reciprocal for bf16 terms) and IEEE division for tiny terms
+ * -- with IEEE division x / world rounded to nearest even (two NaNs count as
+ * equal).  *mismatches receives the number of differing cases,
+ * *first_mismatch the lowest differing bit pattern (0xFFFFFFFF when none).  Runs on the legacy default stream of the current device and
+ * synchronises it.  Errors: DPRED_E_INVAL, DPRED_E_CUDA.
+ */
+int dpred_selftest_prediv(int32_t world, uint64_t* mismatches, uint32_t* first_mismatch);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,3 +35,15 @@ def test_bounds_selftest_matches_the_build():
     want = -7 if zc.checked_build() else 0
     assert zc.device_status(clear=True) == want
     assert zc.device_status() == 0
+
+
+def test_prediv_matches_ieee_division_on_every_fp32_input():
+    """The flush pre-divides every term by the rank count.  For counts that
+    are not powers of two it uses a division-free quotient (Markstein's
+    correction step); for powers of two a multiply by the exact reciprocal.
+    Both must equal IEEE division rounded to nearest even -- what the oracle
+    computes -- on all 2^32 fp32 inputs (which include every bf16 value),
+    for every rank count the library accepts."""
+    for world in range(1, zc.MAX_WORLD + 1):
+        n, first = zc.selftest_prediv(world)
+        assert n == 0, f"world {world}: {n} inputs differ, first bit pattern {first:#010x}"

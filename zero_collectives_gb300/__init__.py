@@ -9,6 +9,7 @@ memory and streams.
 from __future__ import annotations
 
 import ctypes
+import weakref
 import os
 from dataclasses import dataclass
 
@@ -105,6 +106,7 @@ def lib() -> ctypes.CDLL:
         L.dpred_stream_mixed.argtypes = [vp, ctypes.c_size_t, vp, ctypes.c_size_t, vp]
         L.dpred_selftest_wait_timeout.argtypes = [i64, vp]
         L.dpred_selftest_bounds.argtypes = [vp]
+        L.dpred_selftest_prediv.argtypes = [i32, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint32)]
         L.dpred_host_mapped_pointer.argtypes = [vp, ctypes.POINTER(vp)]
         L.dpred_executor_flush_all_mapped.argtypes = L.dpred_executor_flush_all_from_host.argtypes
         _lib = L
@@ -118,9 +120,10 @@ def _check(rc: int) -> None:
 
 def _dtype_code(t) -> int:
     import torch
-    if t.dtype == torch.bfloat16:
+    dt = t.dtype
+    if dt is torch.bfloat16:
         return BF16
-    if t.dtype == torch.float32:
+    if dt is torch.float32:
         return F32
     raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
 
@@ -128,8 +131,28 @@ def _dtype_code(t) -> int:
 def _stream(stream) -> int:
     import torch
     if stream is None:
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:  # the current stream's handle without building a Stream object
+            return raw(torch._C._cuda_getDevice())
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+_PTRS: dict = {}
+
+
+def _ptr(a: np.ndarray) -> int:
+    """Address of a numpy array's data, remembered per live array (numpy's
+    own .ctypes.data costs microseconds per call).  An entry is used only
+    while the same array object, with the same size, is alive."""
+    e = _PTRS.get(id(a))
+    if e is not None and e[0]() is a and e[1] == a.size:
+        return e[2]
+    if len(_PTRS) > 4096:
+        _PTRS.clear()
+    v = a.ctypes.data
+    _PTRS[id(a)] = (weakref.ref(a), a.size, v)
+    return v
 
 
 def version() -> str:
@@ -246,15 +269,24 @@ class ProbeLog:
 
 
 def _probe_from(p: _Probe, world: int) -> Probe:
-    return Probe(p.flush_index, p.tasks, p.reduced_elems, p.owner_tasks, p.owner_elems,
-                 [p.kept_elems[r] for r in range(world)])
+    return Probe(p.flush_index, p.tasks, p.reduced_elems, p.owner_tasks, p.owner_elems, p.kept_elems[:world])
 
 
 def _tasks_arg(tasks: np.ndarray) -> np.ndarray:
+    if type(tasks) is np.ndarray and tasks.dtype is TASK_DTYPE and tasks.flags.c_contiguous:
+        return tasks
     t = np.ascontiguousarray(tasks)
     if t.dtype != TASK_DTYPE:
         t = np.ascontiguousarray(t.astype(TASK_DTYPE))
     return t
+
+
+def _owner_arg(owner):
+    if owner is None:
+        return None
+    if type(owner) is np.ndarray and owner.dtype == np.int32 and owner.flags.c_contiguous:
+        return owner
+    return np.ascontiguousarray(owner, dtype=np.int32)
 
 
 class DstTable:
@@ -299,25 +331,28 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
     None; dst: DstTable or None (in place).  overlap=True promises that this
     flush shares no byte with the work just before it on the stream
     (DPRED_FLUSH_OVERLAP).  Returns a Probe when probe=True."""
-    if grads.dim() != 2 or grads.stride(1) != 1:
+    shape, strides = grads.shape, grads.stride()
+    if len(shape) != 2 or strides[1] != 1:
         raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
-    world = grads.shape[0]
+    world = shape[0]
     in_dt = _dtype_code(grads)
     out_dt = in_dt if out_dtype is None else out_dtype
-    ld = grads.stride(0) if world > 1 else grads.shape[1]
+    ld = strides[0] if world > 1 else shape[1]
     t = _tasks_arg(tasks)
-    own = None if owner is None else np.ascontiguousarray(owner, dtype=np.int32)
+    own = _owner_arg(owner)
     p = _Probe() if probe else None
     if p is not None:
         p.flush_index = flush_index
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
                                                              workspace.numel() * workspace.element_size())
     flags = (FLUSH_CHECKED if checked else 0) | (FLUSH_OVERLAP if overlap else 0)
-    _check(lib().dpred_flush_bucket(world, in_dt, grads.data_ptr(), ld, t.ctypes.data, len(t),
-                                    None if own is None else own.ctypes.data, 0 if own is None else len(own),
-                                    out_dt, None if dst is None else dst.c, int(pre_div), int(reduce_to_owner),
-                                    flags, None if p is None else ctypes.byref(p), ws_ptr, ws_bytes,
-                                    _stream(stream)))
+    rc = lib().dpred_flush_bucket(world, in_dt, grads.data_ptr(), ld, _ptr(t), len(t),
+                                  None if own is None else _ptr(own), 0 if own is None else len(own),
+                                  out_dt, None if dst is None else dst.c, 1 if pre_div else 0,
+                                  1 if reduce_to_owner else 0, flags, None if p is None else ctypes.byref(p),
+                                  ws_ptr, ws_bytes, _stream(stream))
+    if rc:
+        _check(rc)
     return _probe_from(p, world) if p is not None else None
 
 
@@ -525,6 +560,15 @@ def allgather_schedule_step(schedule: int, bufs, step: int, stream=None):
 def checked_build() -> bool:
     """True when the loaded library is the bounds-checked build."""
     return bool(lib().dpred_checked_build())
+
+
+def selftest_prediv(world: int) -> tuple[int, int]:
+    """(mismatches, lowest mismatching fp32 bit pattern or 0xFFFFFFFF) of the
+    flush's pre-division by `world` against IEEE division, over every fp32
+    input (dpred_selftest_prediv)."""
+    n, f = ctypes.c_uint64(), ctypes.c_uint32()
+    _check(lib().dpred_selftest_prediv(int(world), ctypes.byref(n), ctypes.byref(f)))
+    return int(n.value), int(f.value)
 
 
 def selftest_bounds(stream=None) -> None:

@@ -3,6 +3,7 @@
 // kernels execute.  Every entry point validates everything before enqueuing
 // any device work and reports failures as DPRED_E_* codes, never by aborting.
 #include <algorithm>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -86,8 +87,18 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     out.h.wf = (float)world;
     out.h.inv_w = 1.0f / (float)world;
     out.h.unit_vec = unit_vec;
+    prediv_split(world, &out.h.c_hi, &out.h.c_lo);
     out.in_dt = in_dt;
     out.out_dt = out_dt;
+}
+
+void prediv_split(int world, float* c_hi, float* c_lo) {
+    const double inv = 1.0 / (double)world;
+    int e = 0;
+    const double m = std::frexp(inv, &e);  // inv = m * 2^e, m in [0.5, 1)
+    const double hi = std::ldexp(std::floor(std::ldexp(m, 16)), e - 16);
+    *c_hi = (float)hi;                     // 16 significant bits: exact
+    *c_lo = (float)(inv - hi);             // the difference is exact in double
 }
 
 int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cudaStream_t s, bool pdl) {

@@ -53,10 +53,50 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, bool (&done)[64]) {
 // rank count (bit-identical to dividing), IEEE division by any rank count.
 enum PreDiv : int { PDIV_NONE = 0, PDIV_POW2 = 1, PDIV_DIV = 2 };
 
+// Pre-division of one term in the scalar paths: IEEE division for a rank
+// count that is not a power of two, an exact multiply for a power of two.
 __device__ __forceinline__ float pre_divide(float x, int mode, float wf, float inv_w) {
     if (mode == PDIV_POW2) return __fmul_rn(x, inv_w);
     if (mode == PDIV_DIV) return __fdiv_rn(x, wf);
     return x;
+}
+
+// Division-free pre-division for a rank count w that is not a power of two
+// (the vector paths).  Both forms return x / w rounded to nearest even --
+// bit for bit what IEEE division gives -- for every input except the tiny
+// nonzero ones, 0 < |x| < 2^-120 (prediv_tiny), whose quotient can be
+// subnormal; a vector holding one is reduced again with IEEE division.  The
+// library's self-test checks both forms against IEEE division on every input.
+//
+// bf16 terms (8 significant bits): 1/w = c_hi + c_lo with c_hi holding the
+// leading 16 bits of 1/w and c_lo = RN(1/w - c_hi).  x * c_hi has at most 24
+// significant bits, so it is exact, and RN(x * c_lo + x * c_hi) is one fused
+// step whose operand is within about 2^-40 (relative) of x / w.  For w not a
+// power of two the quotient of an 8-bit significand by w is never closer than
+// about 2^-31 (relative) to a rounding midpoint, so that step rounds the same
+// way as the exact quotient.
+__device__ __forceinline__ float div_rank_count_bf16(float x, float c_hi, float c_lo) {
+    return __fmaf_rn(x, c_lo, __fmul_rn(x, c_hi));
+}
+
+// fp32 terms: Markstein's correction step (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990; J.-M. Muller et al., "Handbook of Floating-Point
+// Arithmetic", division with a fused multiply-add).  With y = RN(1/w),
+// q = RN(x y) lies within one ulp of x/w, the residual r = x - q w is exact in
+// one FMA, and RN(q + r y) is the correctly rounded quotient whenever it is a
+// normal number.  A zero residual (q exact, including signed zeros) and a
+// non-finite one (x infinite or NaN) keep q.
+__device__ __forceinline__ float div_rank_count_f32(float x, float w, float inv_w) {
+    const float q = __fmul_rn(x, inv_w);
+    const float r = __fmaf_rn(-q, w, x);
+    const float q1 = __fmaf_rn(r, inv_w, q);
+    return (r == 0.0f || !isfinite(r)) ? q : q1;
+}
+
+// 0 < |x| < 2^-120: the inputs the division-free forms leave to IEEE division.
+__device__ __forceinline__ bool prediv_tiny(float x) {
+    return (__float_as_uint(x) & 0x7FFFFFFFu) - 1u < 0x037FFFFFu;
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
@@ -99,7 +139,12 @@ struct FlushHeader {
     int32_t pdiv;        // PreDiv
     float wf, inv_w;     // world as float, its reciprocal (exact for powers of two)
     int32_t unit_vec;    // 16-byte vectors per work unit of the vector path
+    float c_hi, c_lo;    // 1/world split for the bf16 division-free quotient (prediv_split)
 };
+
+// The split of 1/world used by div_rank_count_bf16: c_hi = the leading 16
+// significant bits of 1/world, c_lo = RN(1/world - c_hi).
+void prediv_split(int world, float* c_hi, float* c_lo);
 
 constexpr int kInlineTasks = 128;
 constexpr int kInlineDst = 512;
@@ -143,7 +188,7 @@ inline int flush_ctas_per_sm(int w, bool write_heavy) {
 // W=8 kernel's register count moved between 56 and 89 with small source
 // changes, i.e. between 4 and 2 resident CTAs; an explicit minimum of 1 also
 // changes the allocation, so the other world sizes pass 0.
-__host__ __device__ constexpr int flush_min_blocks(int w) { return (w == 2 || w == 4 || w == 8) ? flush_ctas_per_sm(w) : 0; }
+__host__ __device__ constexpr int flush_min_blocks(int w) { return (w == 2 || w == 4 || w == 8) ? flush_ctas_per_sm(w) : 2; }
 constexpr int kUnitVec = 256;      // 16-byte vectors per thread-block pass of the vector path (4 KB per row)
 constexpr int kUnitScalar = 2048;  // elements per work unit of the scalar path
 
@@ -161,9 +206,18 @@ struct FlushLaunch {
     bool write_heavy;        // the launch writes at least half as many bytes as it reads
 };
 
-// Vectors each thread keeps in flight per replica row: small world sizes take
-// several so that every SM still has enough bytes outstanding.
-inline int flush_batch(int world) { return world == 2 || world == 3 || world == 4 ? 2 : 1; }
+// World sizes with an unrolled flush kernel of their own; every other world
+// size takes the generic row loop (template world size 0).
+__host__ __device__ constexpr bool flush_specialised(int w) {
+    return w == 2 || w == 3 || w == 4 || w == 5 || w == 6 || w == 7 || w == 8 || w == 12 || w == 16;
+}
+// Vectors each thread keeps in flight per replica row, by template world size
+// (0 = generic, rows in chunks of 4): sized so that a thread has about 8 to 14
+// 16-byte loads outstanding.
+__host__ __device__ constexpr int flush_batch_of(int w_t) {
+    return w_t == 3 ? 3 : (w_t == 2 || w_t == 4 || w_t == 5 || w_t == 6 || w_t == 7 || w_t == 0) ? 2 : 1;
+}
+inline int flush_batch(int world) { return flush_batch_of(flush_specialised(world) ? world : 0); }
 
 // Work units of a plan task; vec_elems = input elements per 16-byte vector,
 // unit_vec = vectors per unit (kUnitVec x the batch).

@@ -107,25 +107,71 @@ __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 #endif
 }
 
-// Fold one replica's vector into the running sums (rank order is the call order).
+// Fold one replica's vector into the running sums (rank order is the call
+// order).  With a rank count that is not a power of two the terms take the
+// division-free quotient, and `tiny` is set when one of them needs IEEE
+// division instead (see prediv_tiny); the caller then reduces the vector
+// again with reduce_vec_ieee.
 template <typename Tin, int MODE>
-__device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q, bool first, float wf, float inv_w) {
+__device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q, bool first, const FlushHeader& h,
+                                     bool& tiny) {
     constexpr int VEC = Elem<Tin>::kVec;
+    constexpr bool kBf16 = std::is_same<Tin, __nv_bfloat16>::value;
     float f[VEC];
     unpack<Tin>(q, f);
 #pragma unroll
     for (int j = 0; j < VEC; ++j) {
-        if constexpr (std::is_same<Tin, __nv_bfloat16>::value && MODE == PDIV_POW2) {
+        if constexpr (kBf16 && MODE == PDIV_POW2) {
             // x * 2^-k is exact for a bf16 x (8 significant bits, lowest bit at
             // 2^-133 or above; 2^-133 * 2^-6 is still a multiple of the smallest
             // fp32 subnormal 2^-149) and 2^k <= 64 ranks.  So rounding
             // x * inv_w + y once gives the bits of rounding y + (x / W): one
             // fused step instead of a multiply and an add.  fp32 inputs keep
             // the two steps, since their quotient can be inexact.
-            y[j] = first ? __fmul_rn(f[j], inv_w) : __fmaf_rn(f[j], inv_w, y[j]);
-        } else {
-            float t = pre_divide(f[j], MODE, wf, inv_w);
+            y[j] = first ? __fmul_rn(f[j], h.inv_w) : __fmaf_rn(f[j], h.inv_w, y[j]);
+        } else if constexpr (MODE == PDIV_DIV) {
+            const float t = kBf16 ? div_rank_count_bf16(f[j], h.c_hi, h.c_lo) : div_rank_count_f32(f[j], h.wf, h.inv_w);
+            tiny |= prediv_tiny(f[j]);
             y[j] = first ? t : __fadd_rn(y[j], t);
+        } else {
+            const float t = pre_divide(f[j], MODE, h.wf, h.inv_w);
+            y[j] = first ? t : __fadd_rn(y[j], t);
+        }
+    }
+}
+
+// The rows of one vector reduced again term by term with IEEE division, for
+// the rare vector that holds a tiny term (rows in global memory, or staged in
+// shared memory row_bytes apart).  One copy per call site, outside the
+// unrolled row loops.
+template <typename Tin>
+__device__ __forceinline__ void reduce_vec_ieee(float (&y)[Elem<Tin>::kVec], const uint4* base, int64_t stride,
+                                                int64_t v, int world, float wf, bool ok) {
+    constexpr int VEC = Elem<Tin>::kVec;
+#pragma unroll 1
+    for (int r = 0; r < world; ++r) {
+        float f[VEC];
+        unpack<Tin>(load_vec(base + (int64_t)r * stride + v, ok), f);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const float t = __fdiv_rn(f[j], wf);
+            y[j] = r == 0 ? t : __fadd_rn(y[j], t);
+        }
+    }
+}
+
+template <typename Tin>
+__device__ __forceinline__ void reduce_vec_ieee_smem(float (&y)[Elem<Tin>::kVec], const unsigned char* tile,
+                                                     size_t row_bytes, int world, float wf) {
+    constexpr int VEC = Elem<Tin>::kVec;
+#pragma unroll 1
+    for (int r = 0; r < world; ++r) {
+        float f[VEC];
+        unpack<Tin>(*reinterpret_cast<const uint4*>(tile + (size_t)r * row_bytes), f);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            const float t = __fdiv_rn(f[j], wf);
+            y[j] = r == 0 ? t : __fadd_rn(y[j], t);
         }
     }
 }
@@ -155,40 +201,57 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
 #pragma unroll 1
     for (int64_t vb = v0 + threadIdx.x; vb < v1; vb += (int64_t)kFlushThreads * BATCH) {
         float y[BATCH][VEC];
+        // Out-of-range vectors of the last pass re-read vector vb (always in
+        // range) instead of branching, and are not stored.
+        int64_t vv[BATCH];
+        bool ok[BATCH], tiny[BATCH];
+#pragma unroll
+        for (int b = 0; b < BATCH; ++b) {
+            vv[b] = vb + (int64_t)b * kFlushThreads < v1 ? vb + (int64_t)b * kFlushThreads : vb;
+            ok[b] = access_ok(vv[b] >= 0 && vv[b] < nbody && T.src_off + T.head + (vv[b] + 1) * VEC <= h.ld, h.err);
+            tiny[b] = false;
+        }
         if constexpr (W_T > 0) {
-            // Out-of-range vectors of the last pass re-read vector vb (always
-            // in range) instead of branching, and are not stored.
             uint4 q[W_T][BATCH];
 #pragma unroll
-            for (int b = 0; b < BATCH; ++b) {
-                const int64_t v = vb + (int64_t)b * kFlushThreads < v1 ? vb + (int64_t)b * kFlushThreads : vb;
-                const bool ok = access_ok(v >= 0 && v < nbody && T.src_off + T.head + (v + 1) * VEC <= h.ld, h.err);
+            for (int b = 0; b < BATCH; ++b)
 #pragma unroll
-                for (int r = 0; r < W_T; ++r) q[r][b] = load_vec(base + r * stride + v, ok);
-            }
+                for (int r = 0; r < W_T; ++r) q[r][b] = load_vec(base + r * stride + vv[b], ok[b]);
 #pragma unroll
             for (int b = 0; b < BATCH; ++b) {
 #pragma unroll
-                for (int r = 0; r < W_T; ++r) fold<Tin, MODE>(y[b], q[r][b], r == 0, h.wf, h.inv_w);
+                for (int r = 0; r < W_T; ++r) fold<Tin, MODE>(y[b], q[r][b], r == 0, h, tiny[b]);
             }
         } else {
-            // Any world size: rows in chunks of 8 loads in flight, folded in rank order.
-            static_assert(BATCH == 1, "generic path keeps one vector per thread");
-            int64_t v = vb;
-            const bool ok = access_ok(v >= 0 && v < nbody && T.src_off + T.head + (v + 1) * VEC <= h.ld, h.err);
-            for (int r0 = 0; r0 < h.world; r0 += 8) {
-                // rows past the last one re-read the last row (no branch around
-                // the loads) and are not folded
-                uint4 q[8];
+            // Any world size: whole chunks of 4 rows, each keeping 4 x BATCH
+            // loads in flight, then the remaining rows one at a time, all
+            // folded in rank order.
+            int r0 = 0;
+#pragma unroll 1
+            for (; r0 + 4 <= h.world; r0 += 4) {
+                uint4 q[4][BATCH];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = r0 + r < h.world ? r0 + r : h.world - 1;
-                    q[r] = load_vec(base + (int64_t)row * stride + v, ok);
-                }
+                for (int r = 0; r < 4; ++r)
 #pragma unroll
-                for (int r = 0; r < 8; ++r)
-                    if (r0 + r < h.world) fold<Tin, MODE>(y[0], q[r], r0 + r == 0, h.wf, h.inv_w);
+                    for (int b = 0; b < BATCH; ++b) q[r][b] = load_vec(base + (int64_t)(r0 + r) * stride + vv[b], ok[b]);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b)
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) fold<Tin, MODE>(y[b], q[r][b], r0 + r == 0, h, tiny[b]);
             }
+#pragma unroll 1
+            for (; r0 < h.world; ++r0) {
+                uint4 q[BATCH];
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) q[b] = load_vec(base + (int64_t)r0 * stride + vv[b], ok[b]);
+#pragma unroll
+                for (int b = 0; b < BATCH; ++b) fold<Tin, MODE>(y[b], q[b], r0 == 0, h, tiny[b]);
+            }
+        }
+        if constexpr (MODE == PDIV_DIV) {
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b)
+                if (tiny[b]) reduce_vec_ieee<Tin>(y[b], base, stride, vv[b], h.world, h.wf, ok[b]);
         }
 #pragma unroll
         for (int b = 0; b < BATCH; ++b) {
@@ -267,19 +330,22 @@ __device__ __forceinline__ uint4 shifted_rt(int s, const uint4& P, const uint4& 
 
 // Reduced, packed source vector v of the task (rows in rank order).
 template <int W_T, typename T, int MODE>
-__device__ __forceinline__ uint4 reduce_packed(const uint4* base, int64_t stride, int64_t v, int world, float wf,
-                                               float inv_w, bool ok) {
+__device__ __forceinline__ uint4 reduce_packed(const uint4* base, int64_t stride, int64_t v, const FlushHeader& h,
+                                               bool ok) {
     constexpr int VEC = Elem<T>::kVec;
     float y[VEC];
+    bool tiny = false;
     if constexpr (W_T > 0) {
         uint4 q[W_T];
 #pragma unroll
         for (int r = 0; r < W_T; ++r) q[r] = load_vec(base + r * stride + v, ok);
 #pragma unroll
-        for (int r = 0; r < W_T; ++r) fold<T, MODE>(y, q[r], r == 0, wf, inv_w);
+        for (int r = 0; r < W_T; ++r) fold<T, MODE>(y, q[r], r == 0, h, tiny);
     } else {
-        for (int r = 0; r < world; ++r) fold<T, MODE>(y, load_vec(base + (int64_t)r * stride + v, ok), r == 0, wf, inv_w);
+        for (int r = 0; r < h.world; ++r) fold<T, MODE>(y, load_vec(base + (int64_t)r * stride + v, ok), r == 0, h, tiny);
     }
+    if constexpr (MODE == PDIV_DIV)
+        if (tiny) reduce_vec_ieee<T>(y, base, stride, v, h.world, h.wf, ok);
     return pack_vec<T>(y);
 }
 
@@ -312,7 +378,7 @@ __device__ __forceinline__ void flush_unit_realign(const Args& a, const TaskDesc
         const int64_t vl = v < v1 ? v : v1 - 1;
         const bool ok = access_ok(vl >= 0 && vl < (Tk.numel - Tk.head) / VEC &&
                                       Tk.src_off + Tk.head + (vl + 1) * VEC <= h.ld, h.err);
-        const uint4 C = reduce_packed<W_T, T, MODE>(base, stride, vl, h.world, h.wf, h.inv_w, ok);
+        const uint4 C = reduce_packed<W_T, T, MODE>(base, stride, vl, h, ok);
         uint4 P;
         P.x = __shfl_up_sync(0xffffffffu, C.x, 1);
         P.y = __shfl_up_sync(0xffffffffu, C.y, 1);
@@ -493,11 +559,14 @@ __device__ void tma_consume(const Args& a, unsigned char* smem, uint64_t* full, 
             if (ctid < nv) {
                 const unsigned char* tile = smem + (size_t)stage * W_T * kTmaRowBytes + (size_t)ctid * 16;
                 float y[VEC];
+                bool tiny = false;
 #pragma unroll
                 for (int r = 0; r < W_T; ++r) {
                     const uint4 q = *reinterpret_cast<const uint4*>(tile + (size_t)r * kTmaRowBytes);
-                    fold<Tin, MODE>(y, q, r == 0, h.wf, h.inv_w);
+                    fold<Tin, MODE>(y, q, r == 0, h, tiny);
                 }
+                if constexpr (MODE == PDIV_DIV)
+                    if (tiny) reduce_vec_ieee_smem<Tin>(y, tile, kTmaRowBytes, W_T, h.wf);
                 const int64_t e = T.head + (sv + ctid) * VEC;
                 if (access_ok(e >= 0 && e + VEC <= T.numel, h.err))
                     for (int d = 0; d < T.ndst; ++d)
@@ -653,6 +722,7 @@ cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_o
 
 template <int W_T, int BATCH, typename Tin, typename Tout>
 int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
+    static_assert(BATCH == flush_batch_of(W_T), "one batch per world size");
     const FlushHeader& h = L.h;
     if (h.total_units == 0) return DPRED_OK;
     cudaError_t e;
@@ -684,20 +754,19 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
     return e == cudaSuccess ? DPRED_OK : cuda_error(e, "flush kernel launch");
 }
 
-template <typename Tin, typename Tout>
-int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
-    switch (L.h.world) {
-        case 2: return launch_flush_w<2, 2, Tin, Tout>(L, s);  // batch = flush_batch(world)
-        case 4: return launch_flush_w<4, 2, Tin, Tout>(L, s);
-        case 8: return launch_flush_w<8, 1, Tin, Tout>(L, s);
-        case 16: return launch_flush_w<16, 1, Tin, Tout>(L, s);
-        // common world sizes that are not powers of two: the same unrolled
-        // body as above instead of the generic row loop
-        case 3: return launch_flush_w<3, 2, Tin, Tout>(L, s);
-        case 6: return launch_flush_w<6, 1, Tin, Tout>(L, s);
-        case 12: return launch_flush_w<12, 1, Tin, Tout>(L, s);
-        default: return launch_flush_w<0, 1, Tin, Tout>(L, s);
-    }
-}
+// Each world size's launchers are compiled in a translation unit of their
+// own (flush_w*.cu, one DPRED_FLUSH_INSTANTIATE line each) so that nvcc builds
+// them in parallel; the dispatcher sees them as extern templates.
+#define DPRED_FLUSH_W_FOR_TYPES(X, W)                                                         \
+    X(W, dpred::flush_batch_of(W), __nv_bfloat16, __nv_bfloat16)                             \
+    X(W, dpred::flush_batch_of(W), __nv_bfloat16, float)                                     \
+    X(W, dpred::flush_batch_of(W), float, float)                                             \
+    X(W, dpred::flush_batch_of(W), float, __nv_bfloat16)
+#define DPRED_FLUSH_INSTANTIATE_ONE(W, B, Tin, Tout) \
+    template int dpred::launch_flush_w<W, B, Tin, Tout>(const dpred::FlushLaunch&, cudaStream_t);
+#define DPRED_FLUSH_DECLARE_ONE(W, B, Tin, Tout) \
+    extern template int dpred::launch_flush_w<W, B, Tin, Tout>(const dpred::FlushLaunch&, cudaStream_t);
+#define DPRED_FLUSH_INSTANTIATE(W) DPRED_FLUSH_W_FOR_TYPES(DPRED_FLUSH_INSTANTIATE_ONE, W)
+#define DPRED_FLUSH_DECLARE(W) DPRED_FLUSH_W_FOR_TYPES(DPRED_FLUSH_DECLARE_ONE, W)
 
 }  // namespace dpred
