@@ -106,16 +106,20 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch():
-    """dram read+write bytes per flush launch from the committed ncu summary,
-    or None when the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "flush_402m_w8_traffic.json")
+def traffic_per_launch(bytes_per_launch: float):
+    """DRAM read+write bytes per flush launch, from the committed ncu record of
+    one bucket-0 launch (805 MB of gradients, one capture, one launch),
+    scaled by the algorithmic bytes of a launch of this run over those of the
+    captured one: every launch of the step streams its W rows once, so its
+    traffic grows in proportion.  None when the kernel sources changed since
+    the capture."""
+    path = os.path.join(ROOT, "profiles", "flush_bucket0_w8_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         if d.get("kernel_hash") != kernel_hash():
             return None
-        return float(d["dram_bytes_per_launch"])
+        return float(d["dram_bytes"]) * bytes_per_launch / float(d["algorithmic_bytes"])
     except Exception:
         return None
 
@@ -270,14 +274,25 @@ def run_dpred(args):
     datagen.fill_device(grads.data_ptr(), WORLD, n_rows, n_rows, BF16, NORMAL, SEED, 0, 1, 0, SIGMA,
                         stream.cuda_stream)
     bucket_list = [(b.start, b.tasks) for b in buckets]
+    # The executor object holds the owner map, the installed gradient buffers
+    # (real on holders, empty elsewhere) and each bucket's destination table;
+    # the timed step flushes through the per-call entry point, one
+    # dpred_flush_bucket call per bucket as the buckets fill, with the probe
+    # counters on and the overlap promise (consecutive buckets share no byte).
     ex = zc.Zero1Executor(WORLD, tree.numel, layout.row_offset, bucket_list, torch.bfloat16)
     step_bytes = flush_bytes(WORLD, buckets, ex.omap, owner_mode_writes(ex.omap))
     step_elems = sum(b.size for b in buckets)
     launches_per_step = len(buckets)
+    calls = [(grads[:, s0:s0 + size], t, tab) for (s0, t), size, tab in zip(ex.buckets, ex.sizes, ex.tables)]
+    owner = ex.omap.owner
+    probes = []
 
     def step():
         zc.build_owner_map(WORLD, [(None, tree.numel)], True)   # the owner map (host, identical every time)
-        ex.flush_all(grads, probe=True)
+        probes.clear()
+        for i, (g, t, tab) in enumerate(calls):
+            probes.append(zc.flush_bucket(g, t, owner, tab, BF16, True, True, probe=True, flush_index=i,
+                                          overlap=True))
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -306,8 +321,7 @@ def run_dpred(args):
     peak, peak_src = peaks()
     bytes_per_launch = step_bytes / launches_per_step
     achieved = bytes_per_launch / (avg_launch_ms * 1e-3) / 1e9
-    # the recorded traffic is per launch of the full 7-bucket workload
-    traffic = traffic_per_launch() if args.max_buckets <= 0 else None
+    traffic = traffic_per_launch(bytes_per_launch)
     result = {
         "metric": METRIC, "value": round(value_gbs, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(elapsed_max / args.steps, 4), "higher_is_better": True,
@@ -338,8 +352,11 @@ def run_dpred(args):
     per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(50))
     result["step_ms_p10_p50_p90"] = [round(per[5], 4), round(per[25], 4), round(per[45], 4)]
     result["replica_elems_per_s"] = round(elems_per_s * WORLD, 1)
-    probe_line = ex.flush_all(grads, probe=True)[0].line(0, zc.BF16, True)
-    result["probe_line"] = probe_line
+    step()
+    torch.cuda.synchronize()
+    result["probe_line"] = probes[0].line(0, zc.BF16, True)
+    result["step_path"] = ("per bucket: dpred_flush_bucket (probe counters on, DPRED_FLUSH_OVERLAP); "
+                           "the owner map rebuilt on the host every step")
     result["owner_map_report"] = ex.omap.report()
 
     if not args.no_e2e:
@@ -528,8 +545,9 @@ def cpu_baseline_all_cores(buckets, tree, seconds=1.5):
 
 
 def flush_path_ab(ex, grads, step_bytes, peak):
-    """The same flush step with each kernel family (LDG streaming vs TMA
-    staging), and with the launch overlap between buckets turned off."""
+    """The same flush step through the native executor (prebuilt plans, one
+    call per step) with each kernel family (LDG streaming vs TMA staging), and
+    with the launch overlap between buckets turned off."""
     import zero_collectives_gb300 as zc
     out = {}
     prev = zc.set_flush_path(zc.PATH_LDG)

@@ -36,14 +36,17 @@ def test_kernel_hash_ignores_comment_edits_but_not_code(tmp_path, monkeypatch):
 
 
 def test_traffic_is_reported_only_for_matching_sources(tmp_path, monkeypatch):
+    """The record holds one bucket-0 launch's DRAM bytes; a launch of another
+    size is scaled by its algorithmic bytes over the captured launch's."""
     csrc = tmp_path / "zero_collectives_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
     for f in bench.KERNEL_SOURCES:
         (csrc / f).write_text("int x = 1;\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    rec = {"kernel_hash": bench.kernel_hash(), "dram_bytes_per_launch": 123.0}
-    (tmp_path / "profiles" / "flush_402m_w8_traffic.json").write_text(json.dumps(rec))
-    assert bench.traffic_per_launch() == 123.0
+    rec = {"kernel_hash": bench.kernel_hash(), "dram_bytes": 900.0, "algorithmic_bytes": 1000.0}
+    (tmp_path / "profiles" / "flush_bucket0_w8_traffic.json").write_text(json.dumps(rec))
+    assert bench.traffic_per_launch(1000.0) == 900.0
+    assert bench.traffic_per_launch(1500.0) == 1350.0
     (csrc / bench.KERNEL_SOURCES[1]).write_text("int x = 3;\n")
-    assert bench.traffic_per_launch() is None
+    assert bench.traffic_per_launch(1000.0) is None
