@@ -167,6 +167,24 @@ int dpred_flush_probe(int32_t world, const dpred_task* tasks, int32_t n_tasks, c
                       int32_t n_params, void* const* dst, int32_t reduce_to_owner, dpred_probe* probe);
 
 /*
+ * The probe line of one flush for one rank ([DS] "Is your feature request
+ * related to a problem? Please describe.": the reduce_probe log line, e.g.
+ * "[dc-probe][r0] flushReduceBucket #3 dtype=BFloat16 tasks=118
+ * reduced_elems=52428800 kept_elems=6553600 discarded=87.5% pre_div=1
+ * owner_tasks=0 owner_elems=0 (0.0%)").  discarded% = 100 * (reduced_elems -
+ * kept_elems[rank]) / reduced_elems and owner% = 100 * owner_elems /
+ * reduced_elems, both with one decimal (0.0 for an empty flush); dtype names
+ * the gradient type ("BFloat16" or "Float").  probe (host) holds the counters
+ * of dpred_flush_probe or dpred_flush_bucket; the NUL-terminated line is
+ * written to buf (host, buf_bytes bytes; 256 always suffice).  Synchronous,
+ * no device work.  Errors: DPRED_E_INVAL (null pointer, world outside
+ * 1..DPRED_MAX_WORLD, rank outside 0..world-1, bad dtype), DPRED_E_SIZE
+ * (buffer too small; buf then holds a truncated line).
+ */
+int dpred_probe_format(const dpred_probe* probe, int32_t world, int32_t rank, int32_t dtype, int32_t pre_div,
+                       char* buf, size_t buf_bytes);
+
+/*
  * Device workspace (bytes) that dpred_flush_bucket may need for a bucket of
  * n_tasks tasks at this world size.  Buckets of up to 128 tasks with up to
  * 512 written destinations travel inside the kernel launch and need none; for

@@ -122,6 +122,18 @@ def test_probe_line_reproduces_printed_line(golden_dir, L):
             else 0 for r in range(world) for t in range(n)]
     pr = zc.flush_probe(world, b.tasks, om.owner, zc.DstTable(world, n, ptrs), False, flush_index=meta["flush_index"])
     assert pr.line(meta["rank"], zc.BF16, True) == line
+    # the same line straight from the C-ABI, and its argument checks
+    raw = zc._Probe()
+    L.dpred_flush_probe(world, b.tasks.ctypes.data, n, om.owner.ctypes.data, len(om.owner),
+                        zc.DstTable(world, n, ptrs).c, 0, ctypes.byref(raw))
+    raw.flush_index = meta["flush_index"]
+    buf = ctypes.create_string_buffer(256)
+    assert L.dpred_probe_format(ctypes.byref(raw), world, meta["rank"], zc.BF16, 1, buf, 256) == 0
+    assert buf.value.decode() == line
+    assert L.dpred_probe_format(ctypes.byref(raw), world, world, zc.BF16, 1, buf, 256) == -1   # rank out of range
+    assert L.dpred_probe_format(ctypes.byref(raw), world, 0, 7, 1, buf, 256) == -1             # bad dtype
+    small = ctypes.create_string_buffer(16)
+    assert L.dpred_probe_format(ctypes.byref(raw), world, 0, zc.BF16, 1, small, 16) == -3      # too small
     log = []
     plog = zc.ProbeLog(rank=0, limit=20, sink=log.append)
     for i in range(25):

@@ -69,6 +69,7 @@ def lib() -> ctypes.CDLL:
         L.dpred_owner_map_digest.argtypes = [i32, vp, vp, vp]
         L.dpred_build_owner_map_device.argtypes = [i32, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp]
         L.dpred_flush_probe.argtypes = [i32, vp, i32, vp, i32, vp, i32, vp]
+        L.dpred_probe_format.argtypes = [vp, i32, i32, i32, i32, ctypes.c_char_p, ctypes.c_size_t]
         L.dpred_flush_workspace_bytes.restype = ctypes.c_size_t
         L.dpred_flush_workspace_bytes.argtypes = [i32, i32]
         L.dpred_flush_bucket.argtypes = [i32, i32, vp, i64, vp, i32, vp, i32, i32, vp, i32, i32, i32, vp, vp,
@@ -241,15 +242,17 @@ class Probe:
     kept_elems: list
 
     def line(self, rank: int, dtype: int, pre_div: bool) -> str:
-        """The probe line of the DeepSpeed issue ("reduce_probe"), for one rank."""
-        red = self.reduced_elems
-        kept = self.kept_elems[rank]
-        disc = 100.0 * (red - kept) / red if red else 0.0
-        own = 100.0 * self.owner_elems / red if red else 0.0
-        return (f"[dc-probe][r{rank}] flushReduceBucket #{self.flush_index} dtype={DTYPE_NAMES[dtype]} "
-                f"tasks={self.tasks} reduced_elems={red} kept_elems={kept} discarded={disc:.1f}% "
-                f"pre_div={int(bool(pre_div))} owner_tasks={self.owner_tasks} owner_elems={self.owner_elems} "
-                f"({own:.1f}%)")
+        """The probe line of the DeepSpeed issue ("reduce_probe"), for one rank,
+        as dpred_probe_format writes it."""
+        p = _Probe()
+        p.flush_index, p.tasks, p.reduced_elems = self.flush_index, self.tasks, self.reduced_elems
+        p.owner_tasks, p.owner_elems = self.owner_tasks, self.owner_elems
+        for r, k in enumerate(self.kept_elems):
+            p.kept_elems[r] = k
+        buf = ctypes.create_string_buffer(256)
+        _check(lib().dpred_probe_format(ctypes.byref(p), len(self.kept_elems), int(rank), int(dtype),
+                                        1 if pre_div else 0, buf, len(buf)))
+        return buf.value.decode()
 
 
 class ProbeLog:

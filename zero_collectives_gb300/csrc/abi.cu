@@ -337,6 +337,27 @@ int dpred_flush_probe(int32_t world, const dpred_task* tasks, int32_t n_tasks, c
     return DPRED_OK;
 }
 
+int dpred_probe_format(const dpred_probe* probe, int32_t world, int32_t rank, int32_t dtype, int32_t pre_div,
+                       char* buf, size_t buf_bytes) {
+    if (!probe || !buf) return set_error(DPRED_E_INVAL, "null probe or buffer");
+    if (world < 1 || world > DPRED_MAX_WORLD) return set_error(DPRED_E_INVAL, "world %d outside 1..%d", world, DPRED_MAX_WORLD);
+    if (rank < 0 || rank >= world) return set_error(DPRED_E_INVAL, "rank %d outside 0..%d", rank, world - 1);
+    if (!dtype_ok(dtype)) return set_error(DPRED_E_INVAL, "bad dtype");
+    const long long red = probe->reduced_elems, kept = probe->kept_elems[rank];
+    const double discarded = red ? 100.0 * (double)(red - kept) / (double)red : 0.0;
+    const double owner_pct = red ? 100.0 * (double)probe->owner_elems / (double)red : 0.0;
+    const int n = std::snprintf(buf, buf_bytes,
+                                "[dc-probe][r%d] flushReduceBucket #%lld dtype=%s tasks=%lld reduced_elems=%lld "
+                                "kept_elems=%lld discarded=%.1f%% pre_div=%d owner_tasks=%lld owner_elems=%lld (%.1f%%)",
+                                rank, (long long)probe->flush_index, dtype == DPRED_BF16 ? "BFloat16" : "Float",
+                                (long long)probe->tasks, red, kept, discarded, pre_div ? 1 : 0,
+                                (long long)probe->owner_tasks, (long long)probe->owner_elems, owner_pct);
+    if (n < 0) return set_error(DPRED_E_INVAL, "probe line formatting failed");
+    if ((size_t)n >= buf_bytes)
+        return set_error(DPRED_E_SIZE, "probe line needs %d bytes plus the terminator, buffer holds %zu", n, buf_bytes);
+    return DPRED_OK;
+}
+
 size_t dpred_flush_workspace_bytes(int32_t world, int32_t n_tasks) {
     if (world < 1 || n_tasks < 0) return 0;
     const int64_t dsts = (int64_t)world * n_tasks;
