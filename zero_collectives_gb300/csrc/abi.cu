@@ -35,7 +35,7 @@ void build_plan(int world, int in_dt, const void* grads, int64_t ld, int out_dt,
     int64_t read_bytes = 0, write_bytes = 0;
     out.tasks.reserve(tasks.size());
     int64_t units = 0;
-    const int unit_vec = kUnitVec * flush_batch(world);
+    const int unit_vec = kUnitVec * flush_batch(world, in_dt == DPRED_BF16);
     for (const Dest& d : tasks) {
         if (d.numel == 0 || d.ptrs.empty()) continue;
         TaskDesc t{};

@@ -212,12 +212,24 @@ __host__ __device__ constexpr bool flush_specialised(int w) {
     return w == 2 || w == 3 || w == 4 || w == 5 || w == 6 || w == 7 || w == 8 || w == 12 || w == 16;
 }
 // Vectors each thread keeps in flight per replica row, by template world size
-// (0 = generic, rows in chunks of 4): sized so that a thread has about 8 to 14
-// 16-byte loads outstanding.
-__host__ __device__ constexpr int flush_batch_of(int w_t) {
-    return w_t == 3 ? 3 : (w_t == 2 || w_t == 4 || w_t == 5 || w_t == 6 || w_t == 7 || w_t == 0) ? 2 : 1;
+// (0 = generic, rows in chunks of 4) and input type: sized so that a thread has
+// about 8 to 21 16-byte loads outstanding.  Interleaved A/B at 256 MB per
+// replica, fraction of the copy peak by batch:
+//   W=3 bf16  3 / 4 / 6 = 0.807 / 0.850 / 0.816;  fp32 3 / 4 / 6 = 0.920 / 0.889 / 0.909
+//   W=5 bf16  2 / 3 / 4 = 0.845 / 0.864 / 0.880;  fp32 = 0.924 / 0.946 / 0.970
+//   W=6 bf16  2 / 3 = 0.874 / 0.899;  fp32 0.938 / 0.953
+//   W=7 bf16  2 / 3 = 0.894 / 0.922;  fp32 0.933 / 0.960
+//   generic (W=9) bf16 2 / 3 = 0.787 / 0.748 (3 spills);  fp32 0.838 / 0.885
+__host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
+    return w_t == 3 ? (bf16_in ? 4 : 3)
+         : w_t == 5 ? 4
+         : (w_t == 6 || w_t == 7) ? 3
+         : w_t == 0 ? (bf16_in ? 2 : 3)
+         : (w_t == 2 || w_t == 4) ? 2 : 1;
 }
-inline int flush_batch(int world) { return flush_batch_of(flush_specialised(world) ? world : 0); }
+inline int flush_batch(int world, bool bf16_in) {
+    return flush_batch_of(flush_specialised(world) ? world : 0, bf16_in);
+}
 
 // Work units of a plan task; vec_elems = input elements per 16-byte vector,
 // unit_vec = vectors per unit (kUnitVec x the batch).

@@ -19,17 +19,18 @@ namespace {
 
 template <typename Tin, typename Tout>
 int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
+    constexpr bool kBf16 = std::is_same<Tin, __nv_bfloat16>::value;
     switch (L.h.world) {
-        case 2: return launch_flush_w<2, flush_batch_of(2), Tin, Tout>(L, s);
-        case 3: return launch_flush_w<3, flush_batch_of(3), Tin, Tout>(L, s);
-        case 4: return launch_flush_w<4, flush_batch_of(4), Tin, Tout>(L, s);
-        case 5: return launch_flush_w<5, flush_batch_of(5), Tin, Tout>(L, s);
-        case 6: return launch_flush_w<6, flush_batch_of(6), Tin, Tout>(L, s);
-        case 7: return launch_flush_w<7, flush_batch_of(7), Tin, Tout>(L, s);
-        case 8: return launch_flush_w<8, flush_batch_of(8), Tin, Tout>(L, s);
-        case 12: return launch_flush_w<12, flush_batch_of(12), Tin, Tout>(L, s);
-        case 16: return launch_flush_w<16, flush_batch_of(16), Tin, Tout>(L, s);
-        default: return launch_flush_w<0, flush_batch_of(0), Tin, Tout>(L, s);
+        case 2: return launch_flush_w<2, flush_batch_of(2, kBf16), Tin, Tout>(L, s);
+        case 3: return launch_flush_w<3, flush_batch_of(3, kBf16), Tin, Tout>(L, s);
+        case 4: return launch_flush_w<4, flush_batch_of(4, kBf16), Tin, Tout>(L, s);
+        case 5: return launch_flush_w<5, flush_batch_of(5, kBf16), Tin, Tout>(L, s);
+        case 6: return launch_flush_w<6, flush_batch_of(6, kBf16), Tin, Tout>(L, s);
+        case 7: return launch_flush_w<7, flush_batch_of(7, kBf16), Tin, Tout>(L, s);
+        case 8: return launch_flush_w<8, flush_batch_of(8, kBf16), Tin, Tout>(L, s);
+        case 12: return launch_flush_w<12, flush_batch_of(12, kBf16), Tin, Tout>(L, s);
+        case 16: return launch_flush_w<16, flush_batch_of(16, kBf16), Tin, Tout>(L, s);
+        default: return launch_flush_w<0, flush_batch_of(0, kBf16), Tin, Tout>(L, s);
     }
 }
 

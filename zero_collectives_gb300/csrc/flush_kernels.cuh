@@ -722,7 +722,8 @@ cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_o
 
 template <int W_T, int BATCH, typename Tin, typename Tout>
 int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
-    static_assert(BATCH == flush_batch_of(W_T), "one batch per world size");
+    static_assert(BATCH == flush_batch_of(W_T, std::is_same<Tin, __nv_bfloat16>::value),
+                  "one batch per world size and input type");
     const FlushHeader& h = L.h;
     if (h.total_units == 0) return DPRED_OK;
     cudaError_t e;
@@ -758,10 +759,10 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
 // own (flush_w*.cu, one DPRED_FLUSH_INSTANTIATE line each) so that nvcc builds
 // them in parallel; the dispatcher sees them as extern templates.
 #define DPRED_FLUSH_W_FOR_TYPES(X, W)                                                         \
-    X(W, dpred::flush_batch_of(W), __nv_bfloat16, __nv_bfloat16)                             \
-    X(W, dpred::flush_batch_of(W), __nv_bfloat16, float)                                     \
-    X(W, dpred::flush_batch_of(W), float, float)                                             \
-    X(W, dpred::flush_batch_of(W), float, __nv_bfloat16)
+    X(W, dpred::flush_batch_of(W, true), __nv_bfloat16, __nv_bfloat16)                       \
+    X(W, dpred::flush_batch_of(W, true), __nv_bfloat16, float)                               \
+    X(W, dpred::flush_batch_of(W, false), float, float)                                      \
+    X(W, dpred::flush_batch_of(W, false), float, __nv_bfloat16)
 #define DPRED_FLUSH_INSTANTIATE_ONE(W, B, Tin, Tout) \
     template int dpred::launch_flush_w<W, B, Tin, Tout>(const dpred::FlushLaunch&, cudaStream_t);
 #define DPRED_FLUSH_DECLARE_ONE(W, B, Tin, Tout) \
