@@ -368,6 +368,9 @@ def run_dpred(args):
         result["flush_paths"] = flush_path_ab(ex, grads, step_bytes, peak)
         result["flush_bucket_calls_step"] = flush_bucket_calls(ex, grads, step_bytes, peak)
         result["flush_bucket_per_call_overhead"] = per_call_overhead()
+        mix = flush_mix_ceiling(grads, step_bytes, peak)
+        mix["step_frac_of_step_mix"] = round(value_gbs / ws / mix["step_mix"]["GB/s"], 4)
+        result["flush_mix_ceiling"] = mix
         del grads
         result["rows"] = rows(peak)
     if rank == 0:
@@ -586,6 +589,26 @@ def flush_bucket_calls(ex, grads, step_bytes, peak):
     return out
 
 
+def flush_mix_ceiling(grads, step_bytes, peak):
+    """HBM ceilings for the flush step's own traffic, measured by kernels that
+    do nothing else (dpred_stream_mixed): the step's reads (the 6.44 GB of
+    gradient rows) alone, and those reads together with its 1.02 GB of writes,
+    spread evenly and with no store waiting for a load."""
+    import torch
+    import zero_collectives_gb300 as zc
+    read_b = grads.numel() * grads.element_size()
+    write_b = (step_bytes - read_b) // 16 * 16
+    dst = torch.empty(write_b, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name, wb in (("read_only", 0), ("step_mix", write_b)):
+        ms = timed(lambda: zc.stream_mixed(grads, dst, read_bytes=read_b, write_bytes=wb), 10)
+        gbs = (read_b + wb) / (ms * 1e-3) / 1e9
+        out[name] = {"ms": round(ms, 4), "GB/s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                     "read_bytes": read_b, "write_bytes": wb}
+    del dst
+    return out
+
+
 def per_call_overhead():
     """Host cost of one dpred_flush_bucket call on a small bucket (W=8, 16
     tasks, 256 KB of gradients): host time per call over 2000 back-to-back
@@ -644,6 +667,18 @@ def per_call_overhead():
         firsts.append((time.perf_counter() - t0) * 1e6)
     torch.cuda.synchronize()
     out["ctypes_first_call_us_median"] = round(float(np.median(firsts)), 2)
+    # the bare ctypes call: the same 17 arguments with an empty task table
+    # (validated from the plan cache, nothing launched)
+    empty = np.zeros(0, dtype=zc.TASK_DTYPE)
+    noop = (world, zc.BF16, grads.data_ptr(), grads.stride(0), empty.ctypes.data, 0, None, 0, zc.BF16, None, 1, 1,
+            0, ctypes.byref(probe), None, 0, s.cuda_stream)
+    for _ in range(100):
+        L.dpred_flush_bucket(*noop)
+    t0 = time.perf_counter()
+    for _ in range(20000):
+        L.dpred_flush_bucket(*noop)
+    out["ctypes_empty_call_us"] = round((time.perf_counter() - t0) / 20000 * 1e6, 2)
+    out["c_side_and_launch_us"] = round(out["ctypes_premarshalled"]["host_us_per_call"] - out["ctypes_empty_call_us"], 2)
     return out
 
 

@@ -14,7 +14,7 @@ import oracle
 import zero_collectives_gb300 as zc
 from datagen import BF16, F32, NORMAL, workloads
 from tests.gpu_util import TORCH_DT, device_matrix, np_bits, oracle_flush, to_bits
-from tests.helpers import holder_sets, is_sentinel
+from tests.helpers import holder_sets, is_sentinel, oracle_dst
 
 pytestmark = pytest.mark.gpu
 
@@ -209,16 +209,30 @@ def test_identical_replicas_reproduce_exactly():
         assert torch.equal(grads[r, o:o + n].view(torch.int16), row[0, o:o + n].view(torch.int16))
 
 
-def test_402m_w8_full_size_sampled():
-    """The full 402.8M-parameter W=8 bf16 flush (7 buckets, reduce-to-owner),
-    run through the executor exactly as the bench times it."""
+@pytest.mark.parametrize("path", ["calls", "executor"])
+def test_402m_w8_full_size_sampled(path):
+    """The full 402.8M-parameter W=8 bf16 flush (7 buckets, reduce-to-owner)
+    in the configurations the bench times: 7 dpred_flush_bucket calls with the
+    probe counters and the overlap promise (checked on the second step, whose
+    plans come from the plan cache, after the buffers are refilled with NaN),
+    and the executor's one-call step."""
     world, sigma, seed = 8, 1e-3, 3
     tree = workloads.tree_402m()
     layout = workloads.arrival_layout(tree)
     grads = device_matrix(world, tree.total, BF16, NORMAL, seed, sigma=sigma)
     ex = zc.Zero1Executor(world, tree.numel, layout.row_offset, [(b.start, b.tasks) for b in layout.buckets],
                           torch.bfloat16, fill=float("nan"))
-    probes = ex.flush_all(grads, probe=True)
+    if path == "executor":
+        probes = ex.flush_all(grads, probe=True)
+    else:
+        calls = [(grads[:, s0:s0 + size], t, tab) for (s0, t), size, tab in zip(ex.buckets, ex.sizes, ex.tables)]
+        for step in range(2):
+            if step == 1:
+                torch.cuda.synchronize()
+                for buf in ex.grad.buf:
+                    buf.fill_(float("nan"))
+            probes = [zc.flush_bucket(g, t, ex.omap.owner, tab, BF16, True, True, probe=True, flush_index=i,
+                                      overlap=True) for i, (g, t, tab) in enumerate(calls)]
     torch.cuda.synchronize()
     assert zc.device_status() == 0
     om = oracle.owner_map(world, [(list(range(world)), tree.numel)])
@@ -355,3 +369,52 @@ def test_indices_beyond_int32():
         check(b1[r], off1, n1, edge + [n1 - 1 - d for d in range(16)] + list(rng.integers(0, n1, 200)))
     # no element of the long destination was left unwritten
     assert not torch.isnan(b0[g:g + big].float()).any()
+
+
+def test_plan_cache_never_serves_a_stale_plan():
+    """dpred_flush_bucket reuses the validated plan of a repeated call.  A call
+    whose owner values, task table (changed in place, same arrays) or
+    destination table differ in any byte must get its own plan: every result
+    equals the oracle for that call's inputs, and buffers of an earlier table
+    are left alone."""
+    world, seed = 4, 31
+    tree = workloads.tree_tiny(seed=1)
+    b = workloads.arrival_layout(tree, capacity=None).buckets[0]
+    grads = device_matrix(world, tree.total, BF16, NORMAL, seed, sigma=1e-2)
+    host = datagen.host_matrix(world, tree.total, BF16, NORMAL, seed, sigma=1e-2)
+    everyone = [set(range(world)) for _ in range(tree.n_params)]  # every rank has a buffer
+    owner = zc.build_owner_map(world, [(None, tree.numel)], True).owner.copy()
+    tasks = b.tasks.copy()
+
+    def run(sb, label):
+        probe = zc.flush_bucket(grads, tasks, owner, sb.table, BF16, True, True, probe=True)
+        odst = oracle_dst(world, tasks, everyone, True)
+        oprobe = oracle.flush(world, host.copy(), tasks, owner, tree.n_params, odst, BF16, True, True)
+        torch.cuda.synchronize()
+        sb.check_against(odst, tasks, BF16)
+        assert probe.kept_elems == oprobe["kept_elems"], label
+        assert (probe.owner_tasks, probe.owner_elems) == (oprobe["owner_tasks"], oprobe["owner_elems"]), label
+
+    def refill(sb):
+        torch.cuda.synchronize()
+        for buf in sb.buf.values():
+            buf.fill_(float("nan"))
+
+    sb = SlotBuffers(world, tasks, everyone, BF16, BF16, "co")
+    run(sb, "first call")
+    refill(sb)
+    run(sb, "the same call again")
+    owned = owner >= 0
+    assert owned.any()
+    owner[owned] = (owner[owned] + 1) % world          # every owned parameter moves to the next rank
+    refill(sb)
+    run(sb, "owners changed in place")
+    tasks["numel"][0] -= 1                              # the first task shrinks, same array
+    refill(sb)
+    run(sb, "task table changed in place")
+    sb2 = SlotBuffers(world, tasks, everyone, BF16, BF16, "co")
+    refill(sb)
+    run(sb2, "new destination table")
+    torch.cuda.synchronize()
+    assert all(bool(torch.isnan(buf.float()).all()) for buf in sb.buf.values()), "old destinations written"
+    assert zc.device_status() == 0
