@@ -107,7 +107,7 @@ def test_tiny_workload(rto, out_dt, mode):
     run_case(world, [(list(range(world)), tree.numel)], BF16, out_dt, True, rto, mode=mode, seed=2)
 
 
-@pytest.mark.parametrize("world", [2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("world", [*range(2, 18), 24, 33])  # every unrolled size, then the generic loop
 @pytest.mark.parametrize("in_dt,out_dt", [(BF16, BF16), (F32, F32), (BF16, F32), (F32, BF16)])
 def test_sweep_world_dtype_straddlers(world, in_dt, out_dt):
     rng = np.random.default_rng(world * 7 + in_dt * 3 + out_dt)

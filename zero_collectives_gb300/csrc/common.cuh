@@ -206,11 +206,9 @@ struct FlushLaunch {
     bool write_heavy;        // the launch writes at least half as many bytes as it reads
 };
 
-// World sizes with an unrolled flush kernel of their own; every other world
-// size takes the generic row loop (template world size 0).
-__host__ __device__ constexpr bool flush_specialised(int w) {
-    return w == 2 || w == 3 || w == 4 || w == 5 || w == 6 || w == 7 || w == 8 || w == 12 || w == 16;
-}
+// World sizes with an unrolled flush kernel of their own (every size from 2
+// to 16); larger ones take the generic row loop (template world size 0).
+__host__ __device__ constexpr bool flush_specialised(int w) { return w >= 2 && w <= 16; }
 // Vectors each thread keeps in flight per replica row, by template world size
 // (0 = generic, rows in chunks of 4) and input type: sized so that a thread has
 // about 8 to 21 16-byte loads outstanding.  Interleaved A/B at 256 MB per
@@ -219,11 +217,15 @@ __host__ __device__ constexpr bool flush_specialised(int w) {
 //   W=5 bf16  2 / 3 / 4 = 0.845 / 0.864 / 0.880;  fp32 = 0.924 / 0.946 / 0.970
 //   W=6 bf16  2 / 3 = 0.874 / 0.899;  fp32 0.938 / 0.953
 //   W=7 bf16  2 / 3 = 0.894 / 0.922;  fp32 0.933 / 0.960
-//   generic (W=9) bf16 2 / 3 = 0.787 / 0.748 (3 spills);  fp32 0.838 / 0.885
+//   W=9 / 10 / 11 batch 1 / 2: bf16 0.828 / 0.899, 0.838 / 0.908, 0.846 / 0.920;
+//                              fp32 0.920 / 0.974, 0.914 / 0.977, 0.916 / 0.960
+//   W=13-15 keep 1 (2 does not fit 2 CTAs per SM): bf16 0.83-0.86, fp32 0.93
+//   generic (then W=9) bf16 2 / 3 = 0.787 / 0.748 (3 spills);  fp32 0.838 / 0.885
 __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
     return w_t == 3 ? (bf16_in ? 4 : 3)
          : w_t == 5 ? 4
          : (w_t == 6 || w_t == 7) ? 3
+         : (w_t == 9 || w_t == 10 || w_t == 11) ? 2
          : w_t == 0 ? (bf16_in ? 2 : 3)
          : (w_t == 2 || w_t == 4) ? 2 : 1;
 }

@@ -10,7 +10,13 @@ DPRED_FLUSH_DECLARE(5)
 DPRED_FLUSH_DECLARE(6)
 DPRED_FLUSH_DECLARE(7)
 DPRED_FLUSH_DECLARE(8)
+DPRED_FLUSH_DECLARE(9)
+DPRED_FLUSH_DECLARE(10)
+DPRED_FLUSH_DECLARE(11)
 DPRED_FLUSH_DECLARE(12)
+DPRED_FLUSH_DECLARE(13)
+DPRED_FLUSH_DECLARE(14)
+DPRED_FLUSH_DECLARE(15)
 DPRED_FLUSH_DECLARE(16)
 DPRED_FLUSH_DECLARE(0)
 
@@ -28,7 +34,13 @@ int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
         case 6: return launch_flush_w<6, flush_batch_of(6, kBf16), Tin, Tout>(L, s);
         case 7: return launch_flush_w<7, flush_batch_of(7, kBf16), Tin, Tout>(L, s);
         case 8: return launch_flush_w<8, flush_batch_of(8, kBf16), Tin, Tout>(L, s);
+        case 9: return launch_flush_w<9, flush_batch_of(9, kBf16), Tin, Tout>(L, s);
+        case 10: return launch_flush_w<10, flush_batch_of(10, kBf16), Tin, Tout>(L, s);
+        case 11: return launch_flush_w<11, flush_batch_of(11, kBf16), Tin, Tout>(L, s);
         case 12: return launch_flush_w<12, flush_batch_of(12, kBf16), Tin, Tout>(L, s);
+        case 13: return launch_flush_w<13, flush_batch_of(13, kBf16), Tin, Tout>(L, s);
+        case 14: return launch_flush_w<14, flush_batch_of(14, kBf16), Tin, Tout>(L, s);
+        case 15: return launch_flush_w<15, flush_batch_of(15, kBf16), Tin, Tout>(L, s);
         case 16: return launch_flush_w<16, flush_batch_of(16, kBf16), Tin, Tout>(L, s);
         default: return launch_flush_w<0, flush_batch_of(0, kBf16), Tin, Tout>(L, s);
     }
