@@ -27,6 +27,12 @@
  *    16-byte alignment is not required but enables the vectorised path.
  *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default stream).
  *    Device work is enqueued on it and the call returns without waiting.
+ *  - Stream capture: a call whose plan goes to a caller workspace (the
+ *    flush, the partitioned flush and the relayout when their
+ *    *_workspace_bytes() is nonzero) uploads that plan from host memory, and
+ *    refuses a stream that is being captured into a CUDA graph with
+ *    DPRED_E_INVAL before enqueuing anything: the captured copy would read
+ *    the host plan again at every replay.
  *  - Arithmetic of every reduction: each term is widened to fp32, optionally
  *    pre-divided by the number of ranks (IEEE division), and the terms are
  *    summed in fp32 in rank order 0, 1, ..., W-1 starting from the rank-0

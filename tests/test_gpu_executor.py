@@ -2,6 +2,8 @@
 for bit, the probe lines count flushes, and the host-buffer step (pipelined
 host-to-device copies, flushes, device-to-host copies) returns exactly what
 the device path computes."""
+import warnings
+
 import numpy as np
 import pytest
 import torch
@@ -237,3 +239,65 @@ def test_in_place_executor_matches_the_oracle(world, dt, rto, overlap):
         ex.flush_all_mapped(torch.empty(grads.shape, dtype=dt, pin_memory=True),
                             [torch.empty(1, dtype=dt, pin_memory=True) for _ in range(world)], grads)
     ex.close()
+
+
+def test_per_call_capture_replays_and_uploaded_plans_are_refused():
+    """Per-call flushes whose plans travel inside the launches can be captured
+    with the overlap promise and replayed bit for bit.  A flush whose plan
+    needs the workspace uploads it from host memory, which a graph cannot
+    capture: under capture the call is refused before anything is enqueued,
+    and the same call made eagerly works."""
+    world = 8
+    tree = workloads.straddle_tree(world, 20000 * world + 3, 4, pieces=3)
+    layout = workloads.arrival_layout(tree, capacity=tree.total // 3)
+    grads = device_matrix(world, tree.total, BF16, NORMAL, 5, sigma=1e-2)
+    om = zc.build_owner_map(world, [(None, tree.numel)], True)
+    bufs = zc.GradBuffers(world, om, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+    tables = [bufs.dst_table(b.tasks) for b in layout.buckets]
+    assert len(layout.buckets) >= 2
+    assert all(zc.flush_workspace_bytes(world, len(b.tasks)) == 0 for b in layout.buckets)
+
+    def step():
+        for b, tab in zip(layout.buckets, tables):
+            zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, tab, BF16, True, True,
+                            overlap=True)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [b.clone() for b in bufs.buf]
+    for b in bufs.buf:
+        b.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    for r in range(world):
+        assert torch.equal(bufs.buf[r].view(torch.int16), eager[r].view(torch.int16))
+
+    # a 300-task bucket: its plan goes to the workspace
+    sizes = np.array([(i * 53) % 700 + 1 for i in range(300)], np.int64)
+    big = workloads.Tree([f"p{i}" for i in range(len(sizes))], sizes)
+    b = workloads.arrival_layout(big, capacity=None).buckets[0]
+    assert zc.flush_workspace_bytes(world, len(b.tasks)) > 0
+    g2 = device_matrix(world, big.total, BF16, NORMAL, 6, sigma=1e-2)
+    om2 = zc.build_owner_map(world, [(None, big.numel)], True)
+    bufs2 = zc.GradBuffers(world, om2, big.numel, workloads.arrival_layout(big, capacity=None).row_offset,
+                           torch.bfloat16, fill=float("nan"))
+    tab2 = bufs2.dst_table(b.tasks)
+    ws = torch.empty(zc.flush_workspace_bytes(world, len(b.tasks)), dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    refused = torch.cuda.CUDAGraph()
+    with warnings.catch_warnings():  # the capture ends empty, as it should
+        warnings.simplefilter("ignore")
+        with torch.cuda.graph(refused, stream=side):
+            with pytest.raises(zc.DpredError) as err:
+                zc.flush_bucket(g2, b.tasks, om2.owner, tab2, BF16, workspace=ws)
+    assert err.value.code == -1 and "graph" in str(err.value)
+    torch.cuda.synchronize()
+    assert all(bool(torch.isnan(x.float()).all()) for x in bufs2.buf), "the refused call wrote something"
+    zc.flush_bucket(g2, b.tasks, om2.owner, tab2, BF16, workspace=ws)
+    torch.cuda.synchronize()
+    assert not all(bool(torch.isnan(x.float()).all()) for x in bufs2.buf)
+    assert zc.device_status() == 0

@@ -122,6 +122,18 @@ int launch_plan(const BuiltPlan& p, void* workspace, size_t workspace_bytes, cud
 
 int flush_path() { return g_flush_path; }
 
+int refuse_capture_of_upload(cudaStream_t s, const char* what) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return cuda_error(e, "stream capture query");
+    if (cs != cudaStreamCaptureStatusNone)
+        return set_error(DPRED_E_INVAL,
+                         "%s does not fit inside the launch and is uploaded from host memory, which a CUDA graph "
+                         "cannot capture; capture only plans with no workspace",
+                         what);
+    return DPRED_OK;
+}
+
 namespace {
 thread_local std::string t_last_error;
 

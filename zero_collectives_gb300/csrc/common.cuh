@@ -297,6 +297,12 @@ size_t relayout_workspace_bytes(int64_t n_pieces);
 
 int* device_error_word();  // device address of the error word (current device)
 
+// DPRED_OK when `s` is not being captured into a CUDA graph; otherwise
+// DPRED_E_INVAL (what names the plan).  A plan uploaded from host memory must
+// not be captured: the captured copy would read the host plan again at every
+// replay, long after the call that owned it.
+int refuse_capture_of_upload(cudaStream_t s, const char* what);
+
 // Kernel family used by the bucket flush (and ReduceScatter): see dpred_set_flush_path.
 enum FlushPath : int { PATH_AUTO = 0, PATH_LDG = 1, PATH_TMA = 2 };
 int flush_path();

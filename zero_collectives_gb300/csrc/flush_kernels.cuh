@@ -741,6 +741,8 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
                              h.n_tasks, L.n_dst, need, L.workspace_bytes);
         if ((reinterpret_cast<uintptr_t>(L.workspace) & 15) != 0)
             return set_error(DPRED_E_ALIGN, "flush workspace must be 16-byte aligned");
+        const int rc = refuse_capture_of_upload(s, "a flush plan");
+        if (rc != DPRED_OK) return rc;
         char* ws = static_cast<char*>(L.workspace);
         e = cudaMemcpyAsync(ws, L.tasks, tb, cudaMemcpyHostToDevice, s);
         if (e == cudaSuccess && db) e = cudaMemcpyAsync(ws + tb, L.dst, db, cudaMemcpyHostToDevice, s);

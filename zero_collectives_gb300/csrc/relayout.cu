@@ -116,6 +116,8 @@ int launch_copy_plan(const char* src, char* dst, const std::vector<int64_t>& tri
             return set_error(DPRED_E_SIZE, "relayout plan of %zu pieces needs %zu bytes of workspace, got %zu",
                              plan.size(), need, workspace_bytes);
         if (reinterpret_cast<uintptr_t>(workspace) % 16) return set_error(DPRED_E_ALIGN, "workspace must be 16-byte aligned");
+        const int rc = refuse_capture_of_upload(s, "a relayout plan");
+        if (rc != DPRED_OK) return rc;
         e = cudaMemcpyAsync(workspace, plan.data(), need, cudaMemcpyHostToDevice, s);
         if (e != cudaSuccess) return cuda_error(e, "relayout plan copy");
         CopyArgsWs a;
