@@ -160,7 +160,7 @@ def test_in_place(rto, dt):
     assert probe.kept_elems == oprobe["kept_elems"]
 
 
-@pytest.mark.parametrize("world", [2, 3, 4, 8, 16, 64])
+@pytest.mark.parametrize("world", [2, 3, 4, 5, 6, 7, 8, 9, 12, 13, 16, 24, 64])
 def test_every_bf16_pattern(world):
     """All 65,536 bf16 bit patterns (subnormals, signed zeros, infinities,
     NaNs), rotated differently in every replica row, plus a block of columns
@@ -188,6 +188,48 @@ def test_every_bf16_pattern(world):
         return ((b & 0x7F80) == 0x7F80) & ((b & 0x7F) != 0)
 
     same = (got == host) | (nan(got) & nan(host))
+    assert same.all(), f"{int((~same).sum())} elements differ, first at {np.argwhere(~same)[0]}"
+    assert zc.device_status() == 0
+
+
+@pytest.mark.parametrize("world", [3, 6, 7, 12, 13, 24])
+def test_fp32_terms_at_the_bottom_of_the_range(world):
+    """fp32 terms divided by a rank count that is not a power of two: the
+    kernels' division-free quotient leaves tiny terms (0 < |x| < 2^-120) to
+    IEEE division.  Rows mix subnormals, the normals around 2^-120, signed
+    zeros, ordinary values, infinities and NaNs, so that the vector path meets
+    tiny terms in some vectors and none in others; every output must equal the
+    oracle bit for bit (a NaN only has to stay NaN)."""
+    rng = np.random.default_rng(100 + world)
+    n = 64 * 1024 + 13
+    pools = [
+        rng.integers(1, 0x00800000, 4096, dtype=np.uint32),                  # subnormals
+        rng.integers(0x03000000, 0x04000000, 4096, dtype=np.uint32),         # around 2^-120
+        np.array([0x00000000, 0x80000000, 0x7F800000, 0xFF800000, 0x7FC00000], np.uint32),
+        rng.integers(0x38000000, 0x3F800000, 4096, dtype=np.uint32),         # ordinary values
+    ]
+    host = np.empty((world, n), np.uint32)
+    for r in range(world):
+        kind = rng.integers(0, 8, n)
+        vals = np.where(kind == 0, rng.choice(pools[0], n),
+                        np.where(kind == 1, rng.choice(pools[1], n),
+                                 np.where(kind == 2, rng.choice(pools[2], n), rng.choice(pools[3], n))))
+        host[r] = vals | (rng.integers(0, 2, n, dtype=np.uint32) << 31)
+        host[r, : n // 3] = rng.choice(pools[3], n // 3)                      # a stretch without tiny terms
+    grads = torch.from_numpy(host.view(np.int32).copy()).cuda().view(torch.float32)
+    tasks = np.zeros(1, dtype=zc.TASK_DTYPE)
+    tasks["numel"] = n
+    zc.flush_bucket(grads, tasks, None, None, F32, True, False)
+    want = host.view(np.float32).copy()
+    oracle.flush(world, want, tasks, None, 1, None, F32, True, False)
+    torch.cuda.synchronize()
+    got = to_bits(grads)
+    wb = want.view(np.uint32)
+
+    def nan(b):
+        return ((b & 0x7F800000) == 0x7F800000) & ((b & 0x7FFFFF) != 0)
+
+    same = (got == wb) | (nan(got) & nan(wb))
     assert same.all(), f"{int((~same).sum())} elements differ, first at {np.argwhere(~same)[0]}"
     assert zc.device_status() == 0
 
