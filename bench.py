@@ -612,10 +612,11 @@ def flush_mix_ceiling(grads, step_bytes, peak):
 def per_call_overhead():
     """Host cost of one dpred_flush_bucket call on a small bucket (W=8, 16
     tasks, 256 KB of gradients): host time per call over 2000 back-to-back
-    eager calls (perf_counter) through the Python binding and through a
-    pre-marshalled ctypes call, the first call (validation and planning) and
-    a repeated call (plan cache), and the device time per call measured with
-    CUDA events over the same loop."""
+    eager calls (perf_counter) through the Python binding, through a prepared
+    per-bucket call (zc.BucketFlush) with and without the probe, and through a
+    pre-marshalled ctypes call; the first call (validation and planning)
+    against a repeated one (plan cache); and the device time per call measured
+    with CUDA events over the same loop."""
     import ctypes
     import time
 
@@ -639,7 +640,10 @@ def per_call_overhead():
     args = (world, zc.BF16, grads.data_ptr(), grads.stride(0), tasks.ctypes.data, n_tasks, owner.ctypes.data,
             n_tasks, zc.BF16, dst.c, 1, 1, 0, ctypes.byref(probe), None, 0, s.cuda_stream)
     out = {"bucket": f"W={world}, {n_tasks} tasks x {per} bf16 elements ({world * n_tasks * per * 2} bytes read)"}
+    prepared = zc.BucketFlush(grads, tasks, owner, dst)
     for name, fn in (("python_binding", lambda: zc.flush_bucket(grads, tasks, owner, dst, probe=True)),
+                     ("python_prepared_call", lambda: prepared(probe=True)),
+                     ("python_prepared_call_no_probe", lambda: prepared()),
                      ("ctypes_premarshalled", lambda: L.dpred_flush_bucket(*args))):
         for _ in range(50):
             fn()

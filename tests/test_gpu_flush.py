@@ -460,3 +460,31 @@ def test_plan_cache_never_serves_a_stale_plan():
     torch.cuda.synchronize()
     assert all(bool(torch.isnan(buf.float()).all()) for buf in sb.buf.values()), "old destinations written"
     assert zc.device_status() == 0
+
+
+def test_prepared_call_matches_flush_bucket():
+    """zc.BucketFlush marshals a bucket's arguments once; every call gives the
+    bits and probe counters of the plain call, step after step, with and
+    without the overlap promise."""
+    world = 8
+    tree = workloads.straddle_tree(world, 30000 * world + 5, 5, pieces=3)
+    layout = workloads.arrival_layout(tree, capacity=tree.total // 2)
+    grads = device_matrix(world, tree.total, BF16, NORMAL, 8, sigma=1e-2)
+    om = zc.build_owner_map(world, [(None, tree.numel)], True)
+    want = zc.GradBuffers(world, om, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+    got = zc.GradBuffers(world, om, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+    probes_want = [zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, want.dst_table(b.tasks),
+                                   BF16, probe=True) for b in layout.buckets]
+    calls = [zc.BucketFlush(grads[:, b.start:b.start + b.size], b.tasks, om.owner, got.dst_table(b.tasks),
+                            overlap=overlap) for b, overlap in zip(layout.buckets, (False, True, True))]
+    for step in range(3):
+        torch.cuda.synchronize()
+        for buf in got.buf:
+            buf.fill_(float("nan"))
+        probes = [c(probe=True, flush_index=i) for i, c in enumerate(calls)]
+        torch.cuda.synchronize()
+        for r in range(world):
+            assert torch.equal(got.buf[r].view(torch.int16), want.buf[r].view(torch.int16)), f"step {step} rank {r}"
+        for p, q in zip(probes, probes_want):
+            assert (p.kept_elems, p.owner_elems, p.reduced_elems) == (q.kept_elems, q.owner_elems, q.reduced_elems)
+    assert zc.device_status() == 0

@@ -359,6 +359,49 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
     return _probe_from(p, world) if p is not None else None
 
 
+class BucketFlush:
+    """One bucket's dpred_flush_bucket call with every argument marshalled
+    once: the gradient view, the task table, the owner map, the destination
+    table and the options.  A caller that flushes the same bucket every step
+    keeps one per bucket; calling it passes only the stream and, when asked,
+    a probe, and the library's plan cache serves the validated plan.  The
+    arrays it was built from must not be changed afterwards (build a new
+    object instead)."""
+
+    def __init__(self, grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
+                 pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False, overlap: bool = False,
+                 workspace=None):
+        shape, strides = grads.shape, grads.stride()
+        if len(shape) != 2 or strides[1] != 1:
+            raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
+        self.world = shape[0]
+        in_dt = _dtype_code(grads)
+        self._tasks = _tasks_arg(tasks).copy()
+        self._owner = None if owner is None else np.array(owner, dtype=np.int32, copy=True)
+        self._dst = dst
+        self._workspace = workspace
+        flags = (FLUSH_CHECKED if checked else 0) | (FLUSH_OVERLAP if overlap else 0)
+        ld = strides[0] if self.world > 1 else shape[1]
+        self._fn = lib().dpred_flush_bucket
+        self._head = (self.world, in_dt, grads.data_ptr(), ld, self._tasks.ctypes.data, len(self._tasks),
+                      None if self._owner is None else self._owner.ctypes.data,
+                      0 if self._owner is None else len(self._owner), in_dt if out_dtype is None else out_dtype,
+                      None if dst is None else dst.c, 1 if pre_div else 0, 1 if reduce_to_owner else 0, flags)
+        self._ws = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                         workspace.numel() * workspace.element_size())
+        self._grads = grads  # keeps the tensor the pointers refer to alive
+
+    def __call__(self, stream=None, probe: bool = False, flush_index: int = 0):
+        p = None
+        if probe:
+            p = _Probe()
+            p.flush_index = flush_index
+        rc = self._fn(*self._head, None if p is None else ctypes.byref(p), *self._ws, _stream(stream))
+        if rc:
+            _check(rc)
+        return _probe_from(p, self.world) if p is not None else None
+
+
 def flush_bucket_noalloc(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
                          pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False,
                          probe: bool = False, flush_index: int = 0, stream=None):
