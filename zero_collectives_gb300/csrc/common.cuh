@@ -229,6 +229,10 @@ __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
          : w_t == 0 ? (bf16_in ? 2 : 3)
          : (w_t == 2 || w_t == 4) ? 2 : 1;
 }
+// A rank count that is not a power of two can reach the kernels of this
+// template world size (the generic loop, or an unrolled size that is not a
+// power of two), so they need the division path.
+__host__ __device__ constexpr bool may_divide(int w_t) { return w_t == 0 || (w_t & (w_t - 1)) != 0; }
 inline int flush_batch(int world, bool bf16_in) {
     return flush_batch_of(flush_specialised(world) ? world : 0, bf16_in);
 }

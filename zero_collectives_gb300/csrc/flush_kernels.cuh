@@ -496,10 +496,12 @@ __global__ void __launch_bounds__(kFlushThreads, flush_min_blocks(W_T)) flush_ke
     for (int64_t u = blockIdx.x; u < h.total_units; u += gridDim.x) {
         const TaskDesc T = plan_task(a, find_task(a, u));
         const int64_t local = u - T.unit_begin;
+        // a power-of-two world size never divides (its pre-division is the
+        // exact multiply), so its kernels carry no division path at all
         if (h.pdiv == PDIV_POW2)
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_POW2, RA>(a, T, local);
-        else if (h.pdiv == PDIV_DIV)
-            flush_unit<W_T, BATCH, Tin, Tout, PDIV_DIV, RA>(a, T, local);
+        else if (may_divide(W_T) && h.pdiv == PDIV_DIV)
+            flush_unit<W_T, BATCH, Tin, Tout, may_divide(W_T) ? PDIV_DIV : PDIV_NONE, RA>(a, T, local);
         else
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE, RA>(a, T, local);
     }
@@ -675,8 +677,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) flush_tma_kernel(const __grid_
     const int mode = a.h.pdiv;
     if (mode == PDIV_POW2)
         tma_consume<W_T, Tin, Tout, PDIV_POW2>(a, smem, full, empty, &abort_flag);
-    else if (mode == PDIV_DIV)
-        tma_consume<W_T, Tin, Tout, PDIV_DIV>(a, smem, full, empty, &abort_flag);
+    else if (may_divide(W_T) && mode == PDIV_DIV)
+        tma_consume<W_T, Tin, Tout, may_divide(W_T) ? PDIV_DIV : PDIV_NONE>(a, smem, full, empty, &abort_flag);
     else
         tma_consume<W_T, Tin, Tout, PDIV_NONE>(a, smem, full, empty, &abort_flag);
 }
