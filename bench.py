@@ -1138,17 +1138,17 @@ def sweep(args):
                     for e, g in zip(exs, gs):
                         e.flush_all(g)
 
-                # the same flushes as direct dpred_flush_bucket calls (plan cache
-                # after the first), with and without the overlap promise (the
-                # copies share no byte)
-                calls = []
-                for e, g in zip(exs, gs):
-                    for (s0, t), size, tab in zip(e.buckets, e.sizes, e.tables):
-                        calls.append((g[:, s0:s0 + size], t, tab, e.omap.owner))
+                # the same flushes as direct dpred_flush_bucket calls, each
+                # bucket's arguments marshalled once (zc.BucketFlush, as a
+                # training loop keeps them; the plan cache serves the plan),
+                # with and without the overlap promise (the copies share no byte)
+                calls = {ov: [zc.BucketFlush(g[:, s0:s0 + size], t, e.omap.owner, tab, code, overlap=ov)
+                              for e, g in zip(exs, gs) for (s0, t), size, tab in zip(e.buckets, e.sizes, e.tables)]
+                         for ov in (False, True)}
 
                 def per_call(overlap):
-                    for g, t, tab, own in calls:
-                        zc.flush_bucket(g, t, own, tab, code, True, True, overlap=overlap)
+                    for c in calls[overlap]:
+                        c()
 
                 side = torch.cuda.Stream()
                 graph = torch.cuda.CUDAGraph()
