@@ -613,8 +613,8 @@ def per_call_overhead():
     """Host cost of one dpred_flush_bucket call on a small bucket (W=8, 16
     tasks, 256 KB of gradients): host time per call over 2000 back-to-back
     eager calls (perf_counter) through the Python binding, through a prepared
-    per-bucket call (zc.BucketFlush) with and without the probe, and through a
-    pre-marshalled ctypes call; the first call (validation and planning)
+    per-bucket call (zc.BucketFlush, by its CPython module and by ctypes) with
+    and without the probe, and through a pre-marshalled ctypes call; the first call (validation and planning)
     against a repeated one (plan cache); and the device time per call measured
     with CUDA events over the same loop."""
     import ctypes
@@ -641,9 +641,13 @@ def per_call_overhead():
             n_tasks, zc.BF16, dst.c, 1, 1, 0, ctypes.byref(probe), None, 0, s.cuda_stream)
     out = {"bucket": f"W={world}, {n_tasks} tasks x {per} bf16 elements ({world * n_tasks * per * 2} bytes read)"}
     prepared = zc.BucketFlush(grads, tasks, owner, dst)
+    prepared_ct = zc.BucketFlush(grads, tasks, owner, dst, fast=False)
+    out["prepared_call_path"] = "cpython module" if prepared.fast else "ctypes (no Python headers on this host)"
     for name, fn in (("python_binding", lambda: zc.flush_bucket(grads, tasks, owner, dst, probe=True)),
                      ("python_prepared_call", lambda: prepared(probe=True)),
                      ("python_prepared_call_no_probe", lambda: prepared()),
+                     ("python_prepared_call_ctypes", lambda: prepared_ct(probe=True)),
+                     ("python_prepared_call_ctypes_no_probe", lambda: prepared_ct()),
                      ("ctypes_premarshalled", lambda: L.dpred_flush_bucket(*args))):
         for _ in range(50):
             fn()

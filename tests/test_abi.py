@@ -200,6 +200,45 @@ def test_empty_calls_are_no_ops(L):
     assert L.dpred_flush_workspace_bytes(2, 200) == 200 * 32 + 2 * 200 * 8
 
 
+def test_prepared_call_paths_agree_without_a_gpu(L):
+    # BucketFlush reaches dpred_flush_bucket through the CPython call module
+    # where it is built (it is here: this Python has headers) or through
+    # ctypes; both give the same probe counters and the same errors.
+    import torch
+    assert zc._fast_call_module() is not None
+    grads = torch.zeros((4, 64), dtype=torch.bfloat16)  # never touched: no call below launches
+    empty = np.zeros(0, dtype=zc.TASK_DTYPE)
+    seen = []
+    for fast in (True, False):
+        bf = zc.BucketFlush(grads, empty, None, None, fast=fast)
+        assert bf.fast is fast
+        assert bf(stream=0) is None
+        seen.append(bf(stream=0, probe=True, flush_index=5))
+    assert seen[0] == seen[1] == zc.Probe(5, 0, 0, 0, 0, [0, 0, 0, 0])
+    errs = []
+    for fast in (True, False):
+        bad = zc.BucketFlush(grads, _tasks([(0, 0, 10)]), [9], None, fast=fast)  # owner 9 is not a rank
+        for probe in (False, True):
+            with pytest.raises(zc.DpredError) as e:
+                bad(stream=0, probe=probe)
+            errs.append((e.value.code, str(e.value)))
+        # checked mode with a destination table: the table reaches the library
+        # (a buffer on a non-owner rank is refused before any launch)
+        tbl = zc.DstTable(4, 1, [0x20000, 0x30000, 0, 0])
+        mis = zc.BucketFlush(grads, _tasks([(0, 0, 10)]), [0], tbl, checked=True, fast=fast)
+        with pytest.raises(zc.DpredError) as e:
+            mis(stream=0)
+        assert e.value.code == -4 and "owned by rank 0" in str(e.value)
+    assert len(set(errs)) == 1 and errs[0][0] == -1
+    fc = zc._fast_call_module()
+    with pytest.raises(ValueError):
+        fc.flush(object(), 0)                 # not a prepared call
+    with pytest.raises(ValueError):
+        fc.prepare(0, *([0] * 15))            # no function address
+    with pytest.raises(TypeError):
+        fc.flush(bf._cap)                     # stream missing
+
+
 def test_owner_map_argument_errors(L):
     own = np.zeros(2, np.int32)
     g = (zc._Group * 1)()

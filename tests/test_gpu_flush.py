@@ -462,10 +462,13 @@ def test_plan_cache_never_serves_a_stale_plan():
     assert zc.device_status() == 0
 
 
-def test_prepared_call_matches_flush_bucket():
+@pytest.mark.parametrize("fast", [True, False], ids=["cpython", "ctypes"])
+def test_prepared_call_matches_flush_bucket(fast):
     """zc.BucketFlush marshals a bucket's arguments once; every call gives the
     bits and probe counters of the plain call, step after step, with and
-    without the overlap promise."""
+    without the overlap promise, through either call path."""
+    if fast and zc._fast_call_module() is None:
+        pytest.skip("the CPython call module is not built on this host (no Python headers)")
     world = 8
     tree = workloads.straddle_tree(world, 30000 * world + 5, 5, pieces=3)
     layout = workloads.arrival_layout(tree, capacity=tree.total // 2)
@@ -476,7 +479,8 @@ def test_prepared_call_matches_flush_bucket():
     probes_want = [zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, want.dst_table(b.tasks),
                                    BF16, probe=True) for b in layout.buckets]
     calls = [zc.BucketFlush(grads[:, b.start:b.start + b.size], b.tasks, om.owner, got.dst_table(b.tasks),
-                            overlap=overlap) for b, overlap in zip(layout.buckets, (False, True, True))]
+                            overlap=overlap, fast=fast) for b, overlap in zip(layout.buckets, (False, True, True))]
+    assert all(c.fast is fast for c in calls)
     for step in range(3):
         torch.cuda.synchronize()
         for buf in got.buf:
@@ -485,6 +489,6 @@ def test_prepared_call_matches_flush_bucket():
         torch.cuda.synchronize()
         for r in range(world):
             assert torch.equal(got.buf[r].view(torch.int16), want.buf[r].view(torch.int16)), f"step {step} rank {r}"
-        for p, q in zip(probes, probes_want):
-            assert (p.kept_elems, p.owner_elems, p.reduced_elems) == (q.kept_elems, q.owner_elems, q.reduced_elems)
+        for i, (p, q) in enumerate(zip(probes, probes_want)):
+            assert p == zc.Probe(i, q.tasks, q.reduced_elems, q.owner_tasks, q.owner_elems, q.kept_elems)
     assert zc.device_status() == 0

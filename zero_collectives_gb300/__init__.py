@@ -359,6 +359,22 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
     return _probe_from(p, world) if p is not None else None
 
 
+_FC = None
+
+
+def _fast_call_module():
+    """The optional CPython call module (built beside the library when this
+    Python has headers), or None; BucketFlush then calls through ctypes."""
+    global _FC
+    if _FC is None:
+        try:
+            from . import _fastcall as fc
+        except ImportError:
+            return None
+        _FC = fc
+    return _FC
+
+
 class BucketFlush:
     """One bucket's dpred_flush_bucket call with every argument marshalled
     once: the gradient view, the task table, the owner map, the destination
@@ -366,11 +382,14 @@ class BucketFlush:
     keeps one per bucket; calling it passes only the stream and, when asked,
     a probe, and the library's plan cache serves the validated plan.  The
     arrays it was built from must not be changed afterwards (build a new
-    object instead)."""
+    object instead).  The call goes through the small CPython module built
+    beside the library where there is one (``fast`` is then True), else
+    through ctypes; ``fast=False`` asks for ctypes.  Both reach the same
+    dpred_flush_bucket in the same loaded library."""
 
     def __init__(self, grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtype: int | None = None,
                  pre_div: bool = True, reduce_to_owner: bool = True, checked: bool = False, overlap: bool = False,
-                 workspace=None):
+                 workspace=None, fast: bool = True):
         shape, strides = grads.shape, grads.stride()
         if len(shape) != 2 or strides[1] != 1:
             raise ValueError("grads must be a 2-D CUDA tensor with unit column stride")
@@ -390,8 +409,27 @@ class BucketFlush:
         self._ws = (None, 0) if workspace is None else (workspace.data_ptr(),
                                                          workspace.numel() * workspace.element_size())
         self._grads = grads  # keeps the tensor the pointers refer to alive
+        fc = _fast_call_module() if fast else None
+        if fc is not None:  # the same arguments as integer addresses (0 = NULL)
+            head = list(self._head)
+            head[9] = 0 if dst is None else ctypes.addressof(dst.c)
+            self._cap = fc.prepare(ctypes.cast(self._fn, ctypes.c_void_p).value,
+                                   *(0 if a is None else a for a in (*head, *self._ws)))
+        else:
+            self._cap = None
+        self.fast = self._cap is not None
 
     def __call__(self, stream=None, probe: bool = False, flush_index: int = 0):
+        if self._cap is not None:
+            if probe:
+                r = _FC.flush_probed(self._cap, _stream(stream), flush_index)
+                if r[0]:
+                    _check(r[0])
+                return Probe(*r[1:])
+            rc = _FC.flush(self._cap, _stream(stream))
+            if rc:
+                _check(rc)
+            return None
         p = None
         if probe:
             p = _Probe()

@@ -9,6 +9,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import os
 import subprocess
+import sysconfig
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
@@ -49,8 +50,39 @@ def _compile(src: str, extra: list[str], objdir: str = OBJDIR) -> str:
     return obj
 
 
+# The optional CPython call path for prepared flushes (argument marshalling
+# only; see csrc/fastcall.c).  Built with the host C compiler when the Python
+# headers are present; without them the binding uses ctypes for the same call.
+FASTCALL = os.path.join(HERE, "_fastcall" + (sysconfig.get_config_var("EXT_SUFFIX") or ".so"))
+
+
+def build_fastcall(force: bool = False) -> str | None:
+    """Compile the fast-call module; returns its path, or None when this
+    Python has no headers or no C compiler (never raises)."""
+    src = os.path.join(CSRC, "fastcall.c")
+    deps = [src, os.path.join(INCLUDE, "dpred.h"), os.path.abspath(__file__)]
+    if not force and os.path.exists(FASTCALL) and all(os.path.getmtime(d) <= os.path.getmtime(FASTCALL) for d in deps):
+        return FASTCALL
+    inc = sysconfig.get_paths().get("include") or ""
+    if not os.path.exists(os.path.join(inc, "Python.h")):
+        return None
+    cc = os.environ.get("CC", "cc")
+    tmp = FASTCALL + ".tmp"
+    try:
+        r = subprocess.run([cc, "-O2", "-shared", "-fPIC", "-std=c11", "-Wall", "-I", inc, "-I", INCLUDE, src, "-o",
+                            tmp], capture_output=True, text=True)
+    except OSError:
+        return None
+    if r.returncode != 0:
+        return None
+    os.replace(tmp, FASTCALL)
+    return FASTCALL
+
+
 def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
     lib, objdir = (LIB_CHECKED, OBJDIR_CHECKED) if checked else (LIB, OBJDIR)
+    if not checked:
+        build_fastcall(force)
     if not force and not stale(lib):
         return lib
     os.makedirs(objdir, exist_ok=True)
