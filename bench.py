@@ -1106,6 +1106,7 @@ def sweep(args):
     import zero_collectives_gb300 as zc
     from datagen import BF16, F32, NORMAL, workloads
     torch.cuda.set_device(0)
+    zc.set_flush_path({"auto": zc.PATH_AUTO, "ldg": zc.PATH_LDG, "tma": zc.PATH_TMA}[args.flush_path])
     peak, _ = peaks()
     s = torch.cuda.current_stream()
     l2 = 129 * 2**20
@@ -1173,7 +1174,7 @@ def sweep(args):
                 ms_o = timed(lambda: per_call(True), reps // copies, warm=3) / copies
                 ms_go = timed(graph_o.replay, reps // copies, warm=3) / copies
                 clk = clocks.stop()
-                line = {"sweep": True, "world": W, "dtype": "bf16" if code == BF16 else "f32",
+                line = {"sweep": True, "flush_path": args.flush_path, "world": W, "dtype": "bf16" if code == BF16 else "f32",
                         "bucket_bytes_per_replica": full.total * esize, "elems": full.total, "copies": copies,
                         "bytes": nbytes, "eager_us": round(ms_e * 1e3, 2), "graph_us": round(ms_g * 1e3, 2),
                         "eager_GBps": round(nbytes / (ms_e * 1e-3) / 1e9, 1),
