@@ -230,6 +230,25 @@ def test_prepared_call_paths_agree_without_a_gpu(L):
             mis(stream=0)
         assert e.value.code == -4 and "owned by rank 0" in str(e.value)
     assert len(set(errs)) == 1 and errs[0][0] == -1
+    # zc.flush_bucket takes the module's one-shot call; forced onto ctypes it
+    # gives the same probe and the same errors
+    got = []
+    for fast in (True, False):
+        with pytest.MonkeyPatch.context() as mp:
+            if not fast:
+                mp.setattr(zc, "_FC", None)
+                mp.setattr(zc, "_fast_call_module", lambda: None)
+            got.append(zc.flush_bucket(grads, empty, None, None, probe=True, flush_index=7, stream=0))
+            assert zc.flush_bucket(grads, empty, None, None, stream=0) is None
+            with pytest.raises(zc.DpredError) as e:
+                zc.flush_bucket(grads, _tasks([(0, 0, 10)]), [9], None, stream=0)
+            got.append((e.value.code, str(e.value)))
+            tbl = zc.DstTable(4, 1, [0x20000, 0x30000, 0, 0])
+            with pytest.raises(zc.DpredError) as e:
+                zc.flush_bucket(grads, _tasks([(0, 0, 10)]), [0], tbl, checked=True, probe=True, stream=0)
+            got.append((e.value.code, str(e.value)))
+    assert got[:3] == got[3:]
+    assert got[0] == zc.Probe(7, 0, 0, 0, 0, [0, 0, 0, 0]) and got[1][0] == -1 and got[2][0] == -4
     fc = zc._fast_call_module()
     with pytest.raises(ValueError):
         fc.flush(object(), 0)                 # not a prepared call
@@ -237,6 +256,10 @@ def test_prepared_call_paths_agree_without_a_gpu(L):
         fc.prepare(0, *([0] * 15))            # no function address
     with pytest.raises(TypeError):
         fc.flush(bf._cap)                     # stream missing
+    with pytest.raises(TypeError):
+        fc.call(0, 4)                         # 18 arguments
+    with pytest.raises(ValueError):
+        fc.call(*([0] * 17), None)            # no function address
 
 
 def test_owner_map_argument_errors(L):

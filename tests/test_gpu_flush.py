@@ -462,6 +462,34 @@ def test_plan_cache_never_serves_a_stale_plan():
     assert zc.device_status() == 0
 
 
+def test_flush_bucket_call_paths_agree(monkeypatch):
+    """zc.flush_bucket goes through the CPython module where it is built;
+    forced onto ctypes, the same buckets give the same bits and probe
+    counters."""
+    if zc._fast_call_module() is None:
+        pytest.skip("the CPython call module is not built on this host (no Python headers)")
+    world = 8
+    tree = workloads.straddle_tree(world, 30000 * world + 5, 5, pieces=3)
+    layout = workloads.arrival_layout(tree, capacity=tree.total // 2)
+    grads = device_matrix(world, tree.total, BF16, NORMAL, 9, sigma=1e-2)
+    om = zc.build_owner_map(world, [(None, tree.numel)], True)
+    bufs = [zc.GradBuffers(world, om, tree.numel, layout.row_offset, torch.bfloat16, fill=float("nan"))
+            for _ in range(2)]
+    probes = []
+    for k, buf in enumerate(bufs):
+        if k == 1:
+            monkeypatch.setattr(zc, "_FC", None)
+            monkeypatch.setattr(zc, "_fast_call_module", lambda: None)
+        probes.append([zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, buf.dst_table(b.tasks),
+                                       BF16, probe=True, flush_index=i) for i, b in enumerate(layout.buckets)])
+    torch.cuda.synchronize()
+    for r in range(world):
+        assert torch.equal(bufs[0].buf[r].view(torch.int16), bufs[1].buf[r].view(torch.int16)), f"rank {r}"
+    assert probes[0] == probes[1]
+    assert [p.flush_index for p in probes[0]] == list(range(len(layout.buckets)))
+    assert zc.device_status() == 0
+
+
 @pytest.mark.parametrize("fast", [True, False], ids=["cpython", "ctypes"])
 def test_prepared_call_matches_flush_bucket(fast):
     """zc.BucketFlush marshals a bucket's arguments once; every call gives the

@@ -302,6 +302,7 @@ class DstTable:
             raise ValueError("dst table must have world * n_tasks entries")
         self.world, self.n_tasks = world, n_tasks
         self.c = (ctypes.c_void_p * max(len(ptrs), 1))(*[p if p else None for p in ptrs])
+        self.addr = ctypes.addressof(self.c)
 
     def nonempty(self) -> np.ndarray:
         return np.array([bool(self.c[i]) for i in range(self.world * self.n_tasks)]).reshape(self.world, self.n_tasks)
@@ -343,12 +344,25 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
     ld = strides[0] if world > 1 else shape[1]
     t = _tasks_arg(tasks)
     own = _owner_arg(owner)
-    p = _Probe() if probe else None
-    if p is not None:
-        p.flush_index = flush_index
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
                                                              workspace.numel() * workspace.element_size())
     flags = (FLUSH_CHECKED if checked else 0) | (FLUSH_OVERLAP if overlap else 0)
+    fc = _FC if _FC is not None else _fast_call_module()
+    if fc is not None:  # the same call through the CPython module (no ctypes conversion)
+        r = fc.call(_flush_fn_address(), world, in_dt, grads.data_ptr(), ld, _ptr(t), len(t),
+                    0 if own is None else _ptr(own), 0 if own is None else len(own), out_dt,
+                    0 if dst is None else dst.addr, 1 if pre_div else 0, 1 if reduce_to_owner else 0, flags,
+                    ws_ptr or 0, ws_bytes, _stream(stream), flush_index if probe else None)
+        if not probe:
+            if r:
+                _check(r)
+            return None
+        if r[0]:
+            _check(r[0])
+        return Probe(*r[1:])
+    p = _Probe() if probe else None
+    if p is not None:
+        p.flush_index = flush_index
     rc = lib().dpred_flush_bucket(world, in_dt, grads.data_ptr(), ld, _ptr(t), len(t),
                                   None if own is None else _ptr(own), 0 if own is None else len(own),
                                   out_dt, None if dst is None else dst.c, 1 if pre_div else 0,
@@ -360,6 +374,14 @@ def flush_bucket(grads, tasks: np.ndarray, owner, dst: DstTable | None, out_dtyp
 
 
 _FC = None
+_FLUSH_FN = None
+
+
+def _flush_fn_address() -> int:
+    global _FLUSH_FN
+    if _FLUSH_FN is None:
+        _FLUSH_FN = ctypes.cast(lib().dpred_flush_bucket, ctypes.c_void_p).value
+    return _FLUSH_FN
 
 
 def _fast_call_module():
