@@ -63,10 +63,11 @@ __device__ __forceinline__ float pre_divide(float x, int mode, float wf, float i
 
 // Division-free pre-division for a rank count w that is not a power of two
 // (the vector paths).  Both forms return x / w rounded to nearest even --
-// bit for bit what IEEE division gives -- for every input except the tiny
-// nonzero ones, 0 < |x| < 2^-120 (prediv_tiny), whose quotient can be
-// subnormal; a vector holding one is reduced again with IEEE division.  The
-// library's self-test checks both forms against IEEE division on every input.
+// bit for bit what IEEE division gives -- for every input except a few tiny
+// ones whose quotient can be subnormal.  Each form flags those (the bf16 form
+// with its own check, the fp32 form with prediv_tiny), and a vector holding a
+// flagged term is reduced again with IEEE division.  The library's self-test
+// checks both forms, checks included, against IEEE division on every input.
 //
 // bf16 terms (8 significant bits): 1/w = c_hi + c_lo with c_hi holding the
 // leading 16 bits of 1/w and c_lo = RN(1/w - c_hi).  x * c_hi has at most 24
@@ -77,6 +78,24 @@ __device__ __forceinline__ float pre_divide(float x, int mode, float wf, float i
 // way as the exact quotient.
 __device__ __forceinline__ float div_rank_count_bf16(float x, float c_hi, float c_lo) {
     return __fmaf_rn(x, c_lo, __fmul_rn(x, c_hi));
+}
+
+// The same quotient with its own check.  The fused step is evaluated a
+// second time with subnormal operands and results flushed to zero.  For a bf16
+// term the two differ exactly when x, the product x * c_hi or the quotient is
+// subnormal, or x is NaN.  Where they agree, the quotient is a normal number
+// (or zero, or infinite) computed from an exact product, and the rounding
+// argument above holds.  Where they differ, `tiny` is set and the caller
+// divides with IEEE division instead.  This check takes two instructions per
+// term (one fused multiply-add, one compare), against three integer
+// instructions for prediv_tiny.
+__device__ __forceinline__ float div_rank_count_bf16_checked(float x, float c_hi, float c_lo, bool& tiny) {
+    const float p = __fmul_rn(x, c_hi);
+    const float t = __fmaf_rn(x, c_lo, p);
+    float tf;
+    asm("fma.rn.ftz.f32 %0, %1, %2, %3;" : "=f"(tf) : "f"(x), "f"(c_lo), "f"(p));
+    tiny |= tf != t;
+    return t;
 }
 
 // fp32 terms: Markstein's correction step (P. Markstein, "Computation of
@@ -94,7 +113,7 @@ __device__ __forceinline__ float div_rank_count_f32(float x, float w, float inv_
     return (r == 0.0f || !isfinite(r)) ? q : q1;
 }
 
-// 0 < |x| < 2^-120: the inputs the division-free forms leave to IEEE division.
+// 0 < |x| < 2^-120: the inputs the fp32 division-free form leaves to IEEE division.
 __device__ __forceinline__ bool prediv_tiny(float x) {
     return (__float_as_uint(x) & 0x7FFFFFFFu) - 1u < 0x037FFFFFu;
 }

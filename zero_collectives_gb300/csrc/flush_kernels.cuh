@@ -130,8 +130,13 @@ __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q
             // the two steps, since their quotient can be inexact.
             y[j] = first ? __fmul_rn(f[j], h.inv_w) : __fmaf_rn(f[j], h.inv_w, y[j]);
         } else if constexpr (MODE == PDIV_DIV) {
-            const float t = kBf16 ? div_rank_count_bf16(f[j], h.c_hi, h.c_lo) : div_rank_count_f32(f[j], h.wf, h.inv_w);
-            tiny |= prediv_tiny(f[j]);
+            float t;
+            if constexpr (kBf16) {
+                t = div_rank_count_bf16_checked(f[j], h.c_hi, h.c_lo, tiny);
+            } else {
+                t = div_rank_count_f32(f[j], h.wf, h.inv_w);
+                tiny |= prediv_tiny(f[j]);
+            }
             y[j] = first ? t : __fadd_rn(y[j], t);
         } else {
             const float t = pre_divide(f[j], MODE, h.wf, h.inv_w);

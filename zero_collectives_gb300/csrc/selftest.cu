@@ -36,8 +36,13 @@ __device__ unsigned int g_prediv_first;  // lowest mismatching bit pattern seen 
 __device__ float vector_prediv(float x, int mode, float w, float inv_w, float c_hi, float c_lo, bool bf16) {
     if (mode == dpred::PDIV_POW2) return __fmul_rn(x, inv_w);
     if (mode == dpred::PDIV_NONE) return x;
+    if (bf16) {
+        bool tiny = false;
+        const float t = dpred::div_rank_count_bf16_checked(x, c_hi, c_lo, tiny);
+        return tiny ? __fdiv_rn(x, w) : t;
+    }
     if (dpred::prediv_tiny(x)) return __fdiv_rn(x, w);
-    return bf16 ? dpred::div_rank_count_bf16(x, c_hi, c_lo) : dpred::div_rank_count_f32(x, w, inv_w);
+    return dpred::div_rank_count_f32(x, w, inv_w);
 }
 
 // Inputs [base, base + gridDim.x * blockDim.x * per): bit pattern u -> float;
