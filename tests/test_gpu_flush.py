@@ -85,8 +85,10 @@ def run_case(world, groups, in_dt, out_dt, pre_div, rto, mode="co", capacity=Non
     holders = holder_sets(om.holder_lo, om.holder_hi)
     for b in layout.buckets:
         sb = SlotBuffers(world, b.tasks, holders, out_dt, in_dt, mode)
+        wsb = zc.flush_workspace_bytes(world, len(b.tasks))  # plans beyond the inline limits (many ranks)
+        ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
         probe = zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, sb.table, out_dt, pre_div,
-                                rto, checked=True, probe=True)
+                                rto, checked=True, probe=True, workspace=ws)
         sub = np.ascontiguousarray(host[:, b.start:b.start + b.size])
         odst, oom, oprobe = oracle_flush(world, sub, b.tasks, numel, groups, out_dt, pre_div, rto, tree.n_params)
         assert np.array_equal(oom["owner"], om.owner)
@@ -107,7 +109,7 @@ def test_tiny_workload(rto, out_dt, mode):
     run_case(world, [(list(range(world)), tree.numel)], BF16, out_dt, True, rto, mode=mode, seed=2)
 
 
-@pytest.mark.parametrize("world", [*range(2, 18), 24, 33])  # every unrolled size, then the generic loop
+@pytest.mark.parametrize("world", [*range(2, 18), 24, 32, 33, 48, 64])  # every unrolled size, then the generic loops
 @pytest.mark.parametrize("in_dt,out_dt", [(BF16, BF16), (F32, F32), (BF16, F32), (F32, BF16)])
 def test_sweep_world_dtype_straddlers(world, in_dt, out_dt):
     rng = np.random.default_rng(world * 7 + in_dt * 3 + out_dt)

@@ -240,6 +240,11 @@ __host__ __device__ constexpr bool flush_specialised(int w) { return w >= 2 && w
 //                              fp32 0.920 / 0.974, 0.914 / 0.977, 0.916 / 0.960
 //   W=13-15 keep 1 (2 does not fit 2 CTAs per SM): bf16 0.83-0.86, fp32 0.93
 //   generic (then W=9) bf16 2 / 3 = 0.787 / 0.748 (3 spills);  fp32 0.838 / 0.885
+//   generic loop, bf16 terms, rows in chunks of 4 with batch 2 against chunks
+//   of 8 with batch 1 (kGenericLarge): W = 17 / 20 / 24 / 28 = 0.827 / 0.870 /
+//   0.886 / 0.894 against 0.798 / 0.831 / 0.890 / 0.867; W = 32 / 40 / 48 / 64
+//   = 0.856 / 0.726 / 0.787 / 0.786 against 1.004 / 0.919 / 0.927 / 0.922.
+//   fp32 terms keep batch 3 and chunks of 4 (batch 2: W = 17-28 lost 4-7%).
 __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
     return w_t == 3 ? (bf16_in ? 4 : 3)
          : w_t == 5 ? 4
@@ -248,13 +253,19 @@ __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
          : w_t == 0 ? (bf16_in ? 2 : 3)
          : (w_t == 2 || w_t == 4) ? 2 : 1;
 }
-// A rank count that is not a power of two can reach the kernels of this
-// template world size (the generic loop, or an unrolled size that is not a
-// power of two), so they need the division path.
-__host__ __device__ constexpr bool may_divide(int w_t) { return w_t == 0 || (w_t & (w_t - 1)) != 0; }
-inline int flush_batch(int world, bool bf16_in) {
-    return flush_batch_of(flush_specialised(world) ? world : 0, bf16_in);
+// Template world size of the generic loop for bf16 terms at kGenericLargeFrom
+// ranks or more: batch 1, rows loaded 8 at a time.
+constexpr int kGenericLarge = -1;
+constexpr int kGenericLargeFrom = 32;
+// The template world size of the kernels that flush `world` ranks.
+__host__ __device__ constexpr int flush_kernel_world(int world, bool bf16_in) {
+    return flush_specialised(world) ? world : (bf16_in && world >= kGenericLargeFrom ? kGenericLarge : 0);
 }
+// A rank count that is not a power of two can reach the kernels of this
+// template world size (the generic loops, or an unrolled size that is not a
+// power of two), so they need the division path.
+__host__ __device__ constexpr bool may_divide(int w_t) { return w_t <= 0 || (w_t & (w_t - 1)) != 0; }
+inline int flush_batch(int world, bool bf16_in) { return flush_batch_of(flush_kernel_world(world, bf16_in), bf16_in); }
 
 // Work units of a plan task; vec_elems = input elements per 16-byte vector,
 // unit_vec = vectors per unit (kUnitVec x the batch).

@@ -246,10 +246,25 @@ __device__ __forceinline__ void flush_unit_vec(const Args& a, const TaskDesc& T,
                 for (int r = 0; r < W_T; ++r) fold<Tin, MODE>(y[b], q[r][b], r == 0, h, tiny[b]);
             }
         } else {
-            // Any world size: whole chunks of 4 rows, each keeping 4 x BATCH
-            // loads in flight, then the remaining rows one at a time, all
-            // folded in rank order.
+            // Any world size: whole chunks of 8 rows (kGenericLarge only) and
+            // of 4 rows, each keeping its loads in flight together, then the
+            // remaining rows one at a time, all folded in rank order.
             int r0 = 0;
+            if constexpr (W_T == kGenericLarge) {
+#pragma unroll 1
+                for (; r0 + 8 <= h.world; r0 += 8) {
+                    uint4 q[8][BATCH];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r)
+#pragma unroll
+                        for (int b = 0; b < BATCH; ++b)
+                            q[r][b] = load_vec(base + (int64_t)(r0 + r) * stride + vv[b], ok[b]);
+#pragma unroll
+                    for (int b = 0; b < BATCH; ++b)
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) fold<Tin, MODE>(y[b], q[r][b], r0 + r == 0, h, tiny[b]);
+                }
+            }
 #pragma unroll 1
             for (; r0 + 4 <= h.world; r0 += 4) {
                 uint4 q[4][BATCH];
@@ -796,5 +811,11 @@ int launch_flush_w(const FlushLaunch& L, cudaStream_t s) {
     extern template int dpred::launch_flush_w<W, B, Tin, Tout>(const dpred::FlushLaunch&, cudaStream_t);
 #define DPRED_FLUSH_INSTANTIATE(W) DPRED_FLUSH_W_FOR_TYPES(DPRED_FLUSH_INSTANTIATE_ONE, W)
 #define DPRED_FLUSH_DECLARE(W) DPRED_FLUSH_W_FOR_TYPES(DPRED_FLUSH_DECLARE_ONE, W)
+// bf16 inputs only (the generic loop for many ranks).
+#define DPRED_FLUSH_W_FOR_BF16_IN(X, W)                                                        \
+    X(W, dpred::flush_batch_of(W, true), __nv_bfloat16, __nv_bfloat16)                       \
+    X(W, dpred::flush_batch_of(W, true), __nv_bfloat16, float)
+#define DPRED_FLUSH_INSTANTIATE_BF16_IN(W) DPRED_FLUSH_W_FOR_BF16_IN(DPRED_FLUSH_INSTANTIATE_ONE, W)
+#define DPRED_FLUSH_DECLARE_BF16_IN(W) DPRED_FLUSH_W_FOR_BF16_IN(DPRED_FLUSH_DECLARE_ONE, W)
 
 }  // namespace dpred
