@@ -253,6 +253,20 @@ __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
          : w_t == 0 ? (bf16_in ? 2 : 3)
          : (w_t == 2 || w_t == 4) ? 2 : 1;
 }
+// Launch one CTA per work unit instead of a persistent grid (the block
+// scheduler then balances the SMs; a persistent grid hands every CTA the same
+// share up front).  Interleaved A/B at 256 MB per replica row, fraction of
+// the copy peak, persistent -> one CTA per unit:
+//   W = 16 bf16 / fp32: 1.030 -> 1.073, 1.033 -> 1.078;
+//   generic loop (w_t = 0): fp32 W = 17 / 24 / 28 / 40 / 48 / 64 = 0.949 / 0.973 /
+//   0.955 / 0.869 / 0.711 / 0.918 -> 0.969 / 1.011 / 1.012 / 1.010 / 1.010 / 1.017,
+//   bf16 W = 17 / 20 / 24 = 0.826 / 0.867 / 0.877 -> 0.832 / 0.876 / 0.887;
+//   chunk-8 loop, powers of two: W = 32 / 64 = 0.985 / 0.904 -> 0.996 / 1.024,
+//   other sizes lost 1-4% (W = 36-56), as did W = 3-14 (2-8%) and W = 8 (18%,
+//   its units carry a quarter of the bytes of a W = 16 unit).
+__host__ __device__ constexpr bool flush_grid_per_unit(int w_t, bool pow2_prediv) {
+    return w_t == 0 || w_t == 16 || (w_t == -1 && pow2_prediv);
+}
 // Template world size of the generic loop for bf16 terms at kGenericLargeFrom
 // ranks or more: batch 1, rows loaded 8 at a time.
 constexpr int kGenericLarge = -1;

@@ -718,8 +718,9 @@ int64_t persistent_grid(K kernel, int64_t units, int max_per_sm) {
 // reach pinned host memory over the host link, and no bulk copy is issued there.
 // Launch of the LDG kernel, with programmatic stream serialisation when pdl.
 template <typename K, typename Args>
-cudaError_t launch_ldg(K k, const Args& a, int64_t units, int max_per_sm, bool pdl, cudaStream_t s) {
-    const unsigned grid = (unsigned)persistent_grid(k, units, max_per_sm);
+cudaError_t launch_ldg(K k, const Args& a, int64_t units, int max_per_sm, bool per_unit, bool pdl, cudaStream_t s) {
+    const unsigned grid = per_unit ? (unsigned)(units < 0x7FFFFFFF ? units : 0x7FFFFFFF)
+                                   : (unsigned)persistent_grid(k, units, max_per_sm);
     if (!pdl) {
         k<<<grid, kFlushThreads, 0, s>>>(a);
         return cudaGetLastError();
@@ -753,11 +754,12 @@ cudaError_t launch_kernel(const Args& a, int64_t units, bool realign, bool ldg_o
             return cudaGetLastError();
         }
     }
+    const bool per_unit = flush_grid_per_unit(W_T, a.h.pdiv == PDIV_POW2);
     if constexpr (std::is_same<Tin, Tout>::value) {
         if (realign)
-            return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, cap, pdl, s);
+            return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, true>, a, units, cap, per_unit, pdl, s);
     }
-    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, cap, pdl, s);
+    return launch_ldg(flush_kernel<W_T, BATCH, Tin, Tout, Args, false>, a, units, cap, per_unit, pdl, s);
 }
 
 template <int W_T, int BATCH, typename Tin, typename Tout>
