@@ -464,6 +464,34 @@ def test_plan_cache_never_serves_a_stale_plan():
     assert zc.device_status() == 0
 
 
+@pytest.mark.parametrize("world,in_dt", [(16, BF16), (24, BF16), (24, F32), (40, BF16), (64, BF16), (48, F32)])
+def test_overlapped_calls_match_plain_calls_at_many_ranks(world, in_dt):
+    """Consecutive flushes with the overlap promise at sizes whose kernels
+    launch one CTA per work unit (W=16, the generic loop, the chunk-8 loop at
+    powers of two) or keep a persistent grid (the chunk-8 loop at other
+    sizes): every bucket's bits equal those of plain, serialised calls (which
+    test_sweep_world_dtype_straddlers checks against the oracle at these
+    sizes)."""
+    dt = TORCH_DT[in_dt]
+    tree = workloads.straddle_tree(world, 20000 * world + 3, world - 1, pieces=3)
+    layout = workloads.arrival_layout(tree, capacity=tree.total // 3)
+    assert len(layout.buckets) >= 3
+    grads = device_matrix(world, tree.total, in_dt, NORMAL, 12, sigma=1e-2)
+    om = zc.build_owner_map(world, [(None, tree.numel)], True)
+    bufs = [zc.GradBuffers(world, om, tree.numel, layout.row_offset, dt, fill=float("nan")) for _ in range(2)]
+    for buf, overlap in zip(bufs, (False, True)):
+        for b in layout.buckets:
+            wsb = zc.flush_workspace_bytes(world, len(b.tasks))
+            ws = torch.empty(wsb, dtype=torch.uint8, device="cuda") if wsb else None
+            zc.flush_bucket(grads[:, b.start:b.start + b.size], b.tasks, om.owner, buf.dst_table(b.tasks), in_dt,
+                            overlap=overlap, workspace=ws)
+    torch.cuda.synchronize()
+    bits = torch.int16 if in_dt == BF16 else torch.int32
+    for r in range(world):
+        assert torch.equal(bufs[0].buf[r].view(bits), bufs[1].buf[r].view(bits)), f"rank {r}"
+    assert zc.device_status() == 0
+
+
 def test_flush_bucket_call_paths_agree(monkeypatch):
     """zc.flush_bucket goes through the CPython module where it is built;
     forced onto ctypes, the same buckets give the same bits and probe
