@@ -51,13 +51,26 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, bool (&done)[64]) {
 
 // Pre-division modes: none, multiply by the exact reciprocal of a power-of-two
 // rank count (bit-identical to dividing), IEEE division by any rank count.
-enum PreDiv : int { PDIV_NONE = 0, PDIV_POW2 = 1, PDIV_DIV = 2 };
+enum PreDiv : int { PDIV_NONE = 0, PDIV_POW2 = 1, PDIV_DIV = 2, PDIV_DIV_EXACT = 3 };
+// PDIV_DIV_EXACT is a compile-time mode of the kernels only (plans carry
+// PDIV_DIV): the division-free quotient without its per-term check, for the
+// unrolled rank counts where that quotient equals IEEE division on every
+// input, subnormal quotients included.
+//  - bf16 terms (split reciprocal): an exhaustive check over the 65,536 bf16
+//    values and every count from 3 to 64 that is not a power of two finds
+//    exactly 3, 5, 15, 17 and 51; the unrolled kernels use 3, 5 and 15.
+//  - fp32 terms (Markstein's step): every odd count from 3 to 15 on all 2^32
+//    inputs.  At an even count a subnormal quotient can fall exactly on a
+//    rounding midpoint, which the step can miss.
+// The library's self-test checks these kernels' quotient on the GPU.
+__host__ __device__ constexpr bool bf16_split_exact(int w) { return w == 3 || w == 5 || w == 15; }
+__host__ __device__ constexpr bool f32_markstein_exact(int w) { return w >= 3 && w <= 15 && (w & 1) != 0; }
 
 // Pre-division of one term in the scalar paths: IEEE division for a rank
 // count that is not a power of two, an exact multiply for a power of two.
 __device__ __forceinline__ float pre_divide(float x, int mode, float wf, float inv_w) {
     if (mode == PDIV_POW2) return __fmul_rn(x, inv_w);
-    if (mode == PDIV_DIV) return __fdiv_rn(x, wf);
+    if (mode == PDIV_DIV || mode == PDIV_DIV_EXACT) return __fdiv_rn(x, wf);
     return x;
 }
 

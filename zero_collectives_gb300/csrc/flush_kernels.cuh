@@ -107,6 +107,17 @@ __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 #endif
 }
 
+// The kernels' mode for a plan that divides: none where the template world
+// size never divides, the unchecked quotient where it is exact for every input
+// of the type (bf16_split_exact, f32_markstein_exact), else the checked one.
+template <typename Tin>
+__host__ __device__ constexpr int div_mode(int w_t) {
+    return !may_divide(w_t) ? PDIV_NONE
+         : (std::is_same<Tin, __nv_bfloat16>::value ? bf16_split_exact(w_t) : f32_markstein_exact(w_t))
+             ? PDIV_DIV_EXACT
+             : PDIV_DIV;
+}
+
 // Fold one replica's vector into the running sums (rank order is the call
 // order).  With a rank count that is not a power of two the terms take the
 // division-free quotient, and `tiny` is set when one of them needs IEEE
@@ -129,6 +140,9 @@ __device__ __forceinline__ void fold(float (&y)[Elem<Tin>::kVec], const uint4& q
             // fused step instead of a multiply and an add.  fp32 inputs keep
             // the two steps, since their quotient can be inexact.
             y[j] = first ? __fmul_rn(f[j], h.inv_w) : __fmaf_rn(f[j], h.inv_w, y[j]);
+        } else if constexpr (MODE == PDIV_DIV_EXACT) {
+            const float t = kBf16 ? div_rank_count_bf16(f[j], h.c_hi, h.c_lo) : div_rank_count_f32(f[j], h.wf, h.inv_w);
+            y[j] = first ? t : __fadd_rn(y[j], t);
         } else if constexpr (MODE == PDIV_DIV) {
             float t;
             if constexpr (kBf16) {
@@ -521,7 +535,7 @@ __global__ void __launch_bounds__(kFlushThreads, flush_min_blocks(W_T)) flush_ke
         if (h.pdiv == PDIV_POW2)
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_POW2, RA>(a, T, local);
         else if (may_divide(W_T) && h.pdiv == PDIV_DIV)
-            flush_unit<W_T, BATCH, Tin, Tout, may_divide(W_T) ? PDIV_DIV : PDIV_NONE, RA>(a, T, local);
+            flush_unit<W_T, BATCH, Tin, Tout, div_mode<Tin>(W_T), RA>(a, T, local);
         else
             flush_unit<W_T, BATCH, Tin, Tout, PDIV_NONE, RA>(a, T, local);
     }
@@ -698,7 +712,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) flush_tma_kernel(const __grid_
     if (mode == PDIV_POW2)
         tma_consume<W_T, Tin, Tout, PDIV_POW2>(a, smem, full, empty, &abort_flag);
     else if (may_divide(W_T) && mode == PDIV_DIV)
-        tma_consume<W_T, Tin, Tout, may_divide(W_T) ? PDIV_DIV : PDIV_NONE>(a, smem, full, empty, &abort_flag);
+        tma_consume<W_T, Tin, Tout, div_mode<Tin>(W_T)>(a, smem, full, empty, &abort_flag);
     else
         tma_consume<W_T, Tin, Tout, PDIV_NONE>(a, smem, full, empty, &abort_flag);
 }
