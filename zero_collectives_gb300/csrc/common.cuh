@@ -251,8 +251,14 @@ __host__ __device__ constexpr bool flush_specialised(int w) { return w >= 2 && w
 //   W=7 bf16  2 / 3 = 0.894 / 0.922;  fp32 0.933 / 0.960
 //   W=9 / 10 / 11 batch 1 / 2: bf16 0.828 / 0.899, 0.838 / 0.908, 0.846 / 0.920;
 //                              fp32 0.920 / 0.974, 0.914 / 0.977, 0.916 / 0.960
-//   W=13-15 keep 1 (2 does not fit 2 CTAs per SM): bf16 0.83-0.86, fp32 0.93
 //   generic (then W=9) bf16 2 / 3 = 0.787 / 0.748 (3 spills);  fp32 0.838 / 0.885
+// Re-run once the division path carried the lighter checks (two instructions
+// per bf16 term, none at the exact counts), batch 1 / 2 at W = 12 / 13 / 14 / 15:
+//   bf16 0.864 / 0.880 / 0.876 / 0.941 -> 0.929 / 0.917 / 0.933 / 0.998;
+//   fp32 0.921 / 0.925 / 0.922 / 0.929 -> 0.975 / 0.986 / 0.981 / 0.997;
+//   bf16 W=9 batch 2 / 3 = 0.912 / 0.932; W=10 / 11 batch 3 lost 0.4 / 0.2
+//   points, W=7 batch 4 lost 1.4, W=6 batch 4 gained 1.0 but spilled (bf16 to
+//   fp32), so those keep their batches.
 //   generic loop, bf16 terms, rows in chunks of 4 with batch 2 against chunks
 //   of 8 with batch 1 (kGenericLarge): W = 17 / 20 / 24 / 28 = 0.827 / 0.870 /
 //   0.886 / 0.894 against 0.798 / 0.831 / 0.890 / 0.867; W = 32 / 40 / 48 / 64
@@ -262,7 +268,9 @@ __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
     return w_t == 3 ? (bf16_in ? 4 : 3)
          : w_t == 5 ? 4
          : (w_t == 6 || w_t == 7) ? 3
-         : (w_t == 9 || w_t == 10 || w_t == 11) ? 2
+         : w_t == 9 ? (bf16_in ? 3 : 2)
+         : (w_t == 10 || w_t == 11) ? 2
+         : (w_t >= 12 && w_t <= 15) ? 2
          : w_t == 0 ? (bf16_in ? 2 : 3)
          : (w_t == 2 || w_t == 4) ? 2 : 1;
 }
