@@ -80,11 +80,17 @@ static PyObject* prepare(PyObject* self, PyObject* args) {
     return cap;
 }
 
+/* The interpreter lock is released around the library call, as ctypes does:
+ * a plan that needs workspace copies it to the device, which can block. */
 static int call(const Prepared* p, dpred_probe* probe, PyObject* stream_arg) {
     const unsigned long long stream = PyLong_AsUnsignedLongLong(stream_arg);
     if (stream == (unsigned long long)-1 && PyErr_Occurred()) return INT32_MIN;
-    return p->fn(p->world, p->in_dt, p->grads, p->ld, p->tasks, p->n_tasks, p->owner, p->n_params, p->out_dt, p->dst,
-                 p->pre_div, p->rto, p->flags, probe, p->workspace, p->workspace_bytes, (void*)(uintptr_t)stream);
+    int rc;
+    Py_BEGIN_ALLOW_THREADS
+    rc = p->fn(p->world, p->in_dt, p->grads, p->ld, p->tasks, p->n_tasks, p->owner, p->n_params, p->out_dt, p->dst,
+               p->pre_div, p->rto, p->flags, probe, p->workspace, p->workspace_bytes, (void*)(uintptr_t)stream);
+    Py_END_ALLOW_THREADS
+    return rc;
 }
 
 /* flush(capsule, stream) -> status code of dpred_flush_bucket */
