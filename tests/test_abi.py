@@ -262,6 +262,35 @@ def test_prepared_call_paths_agree_without_a_gpu(L):
         fc.call(*([0] * 17), None)            # no function address
 
 
+def test_prepared_calls_from_several_threads_keep_their_own_errors(L):
+    # the CPython module releases the interpreter lock during the call; the
+    # library's error text is per thread, so concurrent failing calls each
+    # read their own message
+    import threading
+    import torch
+    grads = torch.zeros((4, 64), dtype=torch.bfloat16)  # never touched: every call fails validation
+    bad = {k: zc.BucketFlush(grads, _tasks([(0, 0, 10)]), [o], None) for k, o in enumerate((4, 5, 6, 7))}
+    seen, errors = {}, []
+
+    def worker(k):
+        try:
+            for _ in range(500):
+                with pytest.raises(zc.DpredError) as e:
+                    bad[k](stream=0)
+                seen.setdefault(k, set()).add(str(e.value))
+        except Exception as exc:  # surfaced below
+            errors.append(exc)
+    threads = [threading.Thread(target=worker, args=(k,)) for k in bad]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors
+    for k, msgs in seen.items():
+        assert len(msgs) == 1, msgs
+        assert str(4 + k) in next(iter(msgs))
+
+
 def test_owner_map_argument_errors(L):
     own = np.zeros(2, np.int32)
     g = (zc._Group * 1)()
