@@ -1,0 +1,44 @@
+"""The bf16 rank counts at which the flush kernels drop their per-term check
+(bf16_split_exact in the library: W = 3, 5 and 15) are exactly those where the
+division-free quotient equals IEEE division on every bf16 input; everywhere
+else the misses are confined to |x| < 2^-120, the range the check sends to
+IEEE division.  Checked on the host from the quotient's definition
+(tests/prediv_exact.c); the GPU self-test checks the kernels' own quotient."""
+import os
+import re
+import shutil
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def table(tmp_path_factory):
+    cc = shutil.which(os.environ.get("CC", "cc")) or shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    exe = str(tmp_path_factory.mktemp("prediv") / "prediv_exact")
+    subprocess.run([cc, "-O2", "-ffp-contract=off", "-fno-fast-math", os.path.join(ROOT, "tests", "prediv_exact.c"),
+                    "-o", exe, "-lm"], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    return {int(w): (int(b), int(bl)) for w, b, bl in (line.split() for line in out.splitlines())}
+
+
+def library_exact_counts():
+    src = open(os.path.join(ROOT, "zero_collectives_gb300", "csrc", "common.cuh")).read()
+    body = re.search(r"constexpr bool bf16_split_exact\(int w\) \{ return ([^;]*);", src).group(1)
+    return {int(v) for v in re.findall(r"w == (\d+)", body)}
+
+
+def test_exact_counts_are_the_libraries(table):
+    exact = {w for w, (bad, _) in table.items() if bad == 0}
+    assert exact == {3, 5, 15, 17, 51}
+    assert library_exact_counts() == exact & set(range(2, 17))  # the unrolled sizes use them
+
+
+def test_misses_stay_below_the_check_threshold(table):
+    assert len(table) == 64 - 2 - 5  # 3..64 without 4, 8, 16, 32, 64
+    assert all(large == 0 for _, large in table.values())
+    assert sum(bad for bad, _ in table.values()) > 0  # the check is needed elsewhere
