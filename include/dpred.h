@@ -646,8 +646,9 @@ int dpred_selftest_bounds(void* stream);
  * compares the quotient the flush kernels' vector paths use for a rank count
  * of `world` -- a multiply by the exact reciprocal for powers of two; for
  * other counts the division-free forms (Markstein's correction for fp32
- * terms, a split reciprocal for bf16 terms) and IEEE division for tiny terms
- * -- with IEEE division x / world rounded to nearest even (two NaNs count as
+ * terms, a split reciprocal for bf16 terms) with IEEE division for the tiny
+ * terms their checks flag (no check at the counts where the form is exact on
+ * every input) -- with IEEE division x / world rounded to nearest even (two NaNs count as
  * equal).  *mismatches receives the number of differing cases,
  * *first_mismatch the lowest differing bit pattern (0xFFFFFFFF when none).  Runs on the legacy default stream of the current device and
  * synchronises it.  Errors: DPRED_E_INVAL, DPRED_E_CUDA.
