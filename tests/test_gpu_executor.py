@@ -170,7 +170,7 @@ def test_mapped_step_rejects_pageable_host_memory():
     ex.close()
 
 
-@pytest.mark.parametrize("world", [2, 8])
+@pytest.mark.parametrize("world", [2, 8, 16, 24, 64])  # persistent grids and one CTA per unit
 def test_overlapped_launches_equal_serial_and_keep_stream_order(world):
     """Consecutive bucket flushes launched with programmatic stream
     serialisation give the serial result bit for bit, and work queued on the
