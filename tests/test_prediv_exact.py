@@ -1,5 +1,5 @@
-"""The bf16 rank counts at which the flush kernels drop their per-term check
-(bf16_split_exact in the library: W = 3, 5 and 15) are exactly those where the
+"""The bf16 rank counts the library lists as exact (bf16_split_exact; its
+kernels drop their per-term check at those below 32) are exactly those where the
 division-free quotient equals IEEE division on every bf16 input; everywhere
 else the misses are confined to |x| < 2^-120, the range the check sends to
 IEEE division.  Checked on the host from the quotient's definition
@@ -35,7 +35,7 @@ def library_exact_counts():
 def test_exact_counts_are_the_libraries(table):
     exact = {w for w, (bad, _) in table.items() if bad == 0}
     assert exact == {3, 5, 15, 17, 51}
-    assert library_exact_counts() == exact & set(range(2, 17))  # the unrolled sizes use them
+    assert library_exact_counts() == exact
 
 
 def test_misses_stay_below_the_check_threshold(table):

@@ -21,7 +21,7 @@ OBJDIR = os.path.join(HERE, "_build")
 # failures recorded as DPRED_E_BOUNDS) is a separate library, built on demand.
 LIB_CHECKED = os.path.join(HERE, "libdpred_checked.so")
 OBJDIR_CHECKED = os.path.join(HERE, "_build_checked")
-FLUSH_UNITS = [f"flush_w{w}.cu" for w in (*(str(w) for w in range(2, 17)), "gen", "gen32")]
+FLUSH_UNITS = [f"flush_w{w}.cu" for w in (*(str(w) for w in range(2, 17)), "gen", "gen32", "genx")]
 SOURCES = ["abi.cu", "flush_dispatch.cu", *FLUSH_UNITS, "accumulate.cu", "allgather.cu", "noalloc.cu", "selftest.cu",
            "relayout.cu", "schedule.cu", "owner_map.cu", "executor.cu", "ceiling.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -53,18 +53,22 @@ cudaError_t ensure_smem_attr(K kernel, int bytes, bool (&done)[64]) {
 // rank count (bit-identical to dividing), IEEE division by any rank count.
 enum PreDiv : int { PDIV_NONE = 0, PDIV_POW2 = 1, PDIV_DIV = 2, PDIV_DIV_EXACT = 3 };
 // PDIV_DIV_EXACT is a compile-time mode of the kernels only (plans carry
-// PDIV_DIV): the division-free quotient without its per-term check, for the
-// unrolled rank counts where that quotient equals IEEE division on every
-// input, subnormal quotients included.
-//  - bf16 terms (split reciprocal): an exhaustive check over the 65,536 bf16
-//    values and every count from 3 to 64 that is not a power of two finds
-//    exactly 3, 5, 15, 17 and 51; the unrolled kernels use 3, 5 and 15.
-//  - fp32 terms (Markstein's step): every odd count from 3 to 15 on all 2^32
-//    inputs.  At an even count a subnormal quotient can fall exactly on a
-//    rounding midpoint, which the step can miss.
-// The library's self-test checks these kernels' quotient on the GPU.
-__host__ __device__ constexpr bool bf16_split_exact(int w) { return w == 3 || w == 5 || w == 15; }
-__host__ __device__ constexpr bool f32_markstein_exact(int w) { return w >= 3 && w <= 15 && (w & 1) != 0; }
+// PDIV_DIV): the division-free quotient without its per-term check, for rank
+// counts where that quotient equals IEEE division on every input, subnormal
+// quotients included.  Exhaustive checks on the host:
+//  - bf16 terms (split reciprocal), all 65,536 bf16 values, every count from 3
+//    to 64 that is not a power of two: exactly 3, 5, 15, 17 and 51;
+//  - fp32 terms (Markstein's step), all 2^32 inputs: every odd count from 3 to
+//    63.  At an even count a subnormal quotient can fall exactly on a rounding
+//    midpoint, which the step can miss.
+__host__ __device__ constexpr bool bf16_split_exact(int w) { return w == 3 || w == 5 || w == 15 || w == 17 || w == 51; }
+__host__ __device__ constexpr bool f32_markstein_exact(int w) { return w >= 3 && w <= 63 && (w & 1) != 0; }
+// The rank counts whose flush kernels use the unchecked quotient: every exact
+// count but bf16 51, which stays on the chunk-8 loop (kGenericLarge) with its
+// check.  The library's self-test checks this quotient at every count.
+__host__ __device__ constexpr bool flush_prediv_unchecked(int w, bool bf16_in) {
+    return bf16_in ? (bf16_split_exact(w) && w < 32) : f32_markstein_exact(w);
+}
 
 // Pre-division of one term in the scalar paths: IEEE division for a rank
 // count that is not a power of two, an exact multiply for a power of two.
@@ -271,7 +275,7 @@ __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
          : w_t == 9 ? (bf16_in ? 3 : 2)
          : (w_t == 10 || w_t == 11) ? 2
          : (w_t >= 12 && w_t <= 15) ? 2
-         : w_t == 0 ? (bf16_in ? 2 : 3)
+         : (w_t == 0 || w_t == -2) ? (bf16_in ? 2 : 3)
          : (w_t == 2 || w_t == 4) ? 2 : 1;
 }
 // Launch one CTA per work unit instead of a persistent grid (the block
@@ -286,15 +290,21 @@ __host__ __device__ constexpr int flush_batch_of(int w_t, bool bf16_in) {
 //   other sizes lost 1-4% (W = 36-56), as did W = 3-14 (2-8%) and W = 8 (18%,
 //   its units carry a quarter of the bytes of a W = 16 unit).
 __host__ __device__ constexpr bool flush_grid_per_unit(int w_t, bool pow2_prediv) {
-    return w_t == 0 || w_t == 16 || (w_t == -1 && pow2_prediv);
+    return w_t == 0 || w_t == -2 || w_t == 16 || (w_t == -1 && pow2_prediv);
 }
 // Template world size of the generic loop for bf16 terms at kGenericLargeFrom
 // ranks or more: batch 1, rows loaded 8 at a time.
 constexpr int kGenericLarge = -1;
 constexpr int kGenericLargeFrom = 32;
+// Template world size of the generic loop (as w_t = 0) for the counts above 16
+// that divide without a check (flush_prediv_unchecked).
+constexpr int kGenericExact = -2;
 // The template world size of the kernels that flush `world` ranks.
 __host__ __device__ constexpr int flush_kernel_world(int world, bool bf16_in) {
-    return flush_specialised(world) ? world : (bf16_in && world >= kGenericLargeFrom ? kGenericLarge : 0);
+    return flush_specialised(world)                 ? world
+         : flush_prediv_unchecked(world, bf16_in)   ? kGenericExact
+         : (bf16_in && world >= kGenericLargeFrom)  ? kGenericLarge
+                                                    : 0;
 }
 // A rank count that is not a power of two can reach the kernels of this
 // template world size (the generic loops, or an unrolled size that is not a

@@ -20,6 +20,7 @@ DPRED_FLUSH_DECLARE(15)
 DPRED_FLUSH_DECLARE(16)
 DPRED_FLUSH_DECLARE(0)
 DPRED_FLUSH_DECLARE_BF16_IN(dpred::kGenericLarge)
+DPRED_FLUSH_DECLARE(dpred::kGenericExact)
 
 namespace dpred {
 namespace {
@@ -43,12 +44,16 @@ int launch_flush_typed(const FlushLaunch& L, cudaStream_t s) {
         case 14: return launch_flush_w<14, flush_batch_of(14, kBf16), Tin, Tout>(L, s);
         case 15: return launch_flush_w<15, flush_batch_of(15, kBf16), Tin, Tout>(L, s);
         case 16: return launch_flush_w<16, flush_batch_of(16, kBf16), Tin, Tout>(L, s);
-        default:
+        default: {
+            const int wk = flush_kernel_world(L.h.world, kBf16);
+            if (wk == kGenericExact)
+                return launch_flush_w<kGenericExact, flush_batch_of(kGenericExact, kBf16), Tin, Tout>(L, s);
             if constexpr (kBf16) {
-                if (flush_kernel_world(L.h.world, true) == kGenericLarge)
+                if (wk == kGenericLarge)
                     return launch_flush_w<kGenericLarge, flush_batch_of(kGenericLarge, true), Tin, Tout>(L, s);
             }
             return launch_flush_w<0, flush_batch_of(0, kBf16), Tin, Tout>(L, s);
+        }
     }
 }
 

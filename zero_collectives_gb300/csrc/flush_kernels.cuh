@@ -108,12 +108,12 @@ __device__ __forceinline__ uint4 load_vec(const uint4* p, bool ok) {
 }
 
 // The kernels' mode for a plan that divides: none where the template world
-// size never divides, the unchecked quotient where it is exact for every input
-// of the type (bf16_split_exact, f32_markstein_exact), else the checked one.
+// size never divides, the unchecked quotient at the counts that take it
+// (flush_prediv_unchecked, and the kGenericExact loop), else the checked one.
 template <typename Tin>
 __host__ __device__ constexpr int div_mode(int w_t) {
     return !may_divide(w_t) ? PDIV_NONE
-         : (std::is_same<Tin, __nv_bfloat16>::value ? bf16_split_exact(w_t) : f32_markstein_exact(w_t))
+         : (w_t == kGenericExact || (w_t > 0 && flush_prediv_unchecked(w_t, std::is_same<Tin, __nv_bfloat16>::value)))
              ? PDIV_DIV_EXACT
              : PDIV_DIV;
 }

@@ -36,8 +36,8 @@ __device__ unsigned int g_prediv_first;  // lowest mismatching bit pattern seen 
 __device__ float vector_prediv(float x, int mode, float w, float inv_w, float c_hi, float c_lo, bool bf16) {
     if (mode == dpred::PDIV_POW2) return __fmul_rn(x, inv_w);
     if (mode == dpred::PDIV_NONE) return x;
-    if (bf16 && dpred::bf16_split_exact((int)w)) return dpred::div_rank_count_bf16(x, c_hi, c_lo);
-    if (!bf16 && dpred::f32_markstein_exact((int)w)) return dpred::div_rank_count_f32(x, w, inv_w);
+    if (dpred::flush_prediv_unchecked((int)w, bf16))
+        return bf16 ? dpred::div_rank_count_bf16(x, c_hi, c_lo) : dpred::div_rank_count_f32(x, w, inv_w);
     if (bf16) {
         bool tiny = false;
         const float t = dpred::div_rank_count_bf16_checked(x, c_hi, c_lo, tiny);
