@@ -23,7 +23,7 @@ def table(tmp_path_factory):
     subprocess.run([cc, "-O2", "-ffp-contract=off", "-fno-fast-math", os.path.join(ROOT, "tests", "prediv_exact.c"),
                     "-o", exe, "-lm"], check=True)
     out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
-    return {int(w): (int(b), int(bl)) for w, b, bl in (line.split() for line in out.splitlines())}
+    return {int(w): (int(b), int(bl), int(bc)) for w, b, bl, bc in (line.split() for line in out.splitlines())}
 
 
 def library_exact_counts():
@@ -33,12 +33,18 @@ def library_exact_counts():
 
 
 def test_exact_counts_are_the_libraries(table):
-    exact = {w for w, (bad, _) in table.items() if bad == 0}
+    exact = {w for w, (bad, _, _) in table.items() if bad == 0}
     assert exact == {3, 5, 15, 17, 51}
     assert library_exact_counts() == exact
 
 
 def test_misses_stay_below_the_check_threshold(table):
     assert len(table) == 64 - 2 - 5  # 3..64 without 4, 8, 16, 32, 64
-    assert all(large == 0 for _, large in table.values())
-    assert sum(bad for bad, _ in table.values()) > 0  # the check is needed elsewhere
+    assert all(large == 0 for _, large, _ in table.values())
+    assert sum(bad for bad, _, _ in table.values()) > 0  # the check is needed elsewhere
+
+
+def test_the_kernels_check_catches_every_miss(table):
+    # the FTZ twin of the fused step, with IEEE division where it disagrees,
+    # gives IEEE division on every bf16 input at every count
+    assert all(checked == 0 for _, _, checked in table.values())
